@@ -1,0 +1,440 @@
+"""Benchmark: MoE token dispatch + combine on GB300 at the DeepSeek-V3 prefill shape.
+
+One step = ep_layout + ep_dispatch (bf16 -> FP8-E4M3, 1x128 fp32 scales, into
+the 128-row-aligned per-expert-contiguous layout) + ep_combine (top-8 weighted
+reduction of bf16 expert outputs), for T=16384 tokens, H=7168, E=256, top-8
+grouped-sigmoid routing.  Inputs are seeded synthetic data resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  N > 1 (under torchrun) runs independent replicas, one per
+GPU, with no collective on the data path ("weak" scaling); a barrier and the
+max over ranks bracket the timed region.  ``--impl reference`` times the CPU
+oracle on the host cores instead (rank 0 only), on token samples of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (fraction of GB300 peak)"
+WORKLOAD = "dsv3_prefill"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "combine_dsv3_prefill_traffic.txt")
+COMBINE_SRC = os.path.join(ROOT, "combine_expert_histogram_gb300", "csrc", "combine.cu")
+
+
+# ----------------------------------------------------------- algorithmic bytes
+def algorithmic_bytes(w: workloads.Workload) -> dict:
+    """Bytes the method must move per launch (padding and empty slots excluded)."""
+    T, H, K = w.T, w.H, w.K
+    G = H // 128
+    row = {"none": 2 * H, "fp8_f32": H + 4 * G, "fp8_ue8m0": H + 4 * ((G + 3) // 4)}[w.quant]
+    return dict(
+        layout=T * (4 * K + 4 * K + 4 * K),               # idx read, dst_row + row_src written
+        dispatch=T * (2 * H + 4 * K + K * row),           # x read, dst_row read, K rows written
+        combine=T * (K * 2 * H + 4 * K + 4 * K + 2 * H),  # K rows + w + dst_row read, out written
+    )
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+            if k in d and d[k]:
+                return float(d[k]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def combine_traffic():
+    """DRAM bytes per combine launch from the committed ncu summary, if it was
+    taken on the current combine.cu (else None)."""
+    try:
+        src_hash = hashlib.sha256(open(COMBINE_SRC, "rb").read()).hexdigest()[:16]
+        kv = {}
+        for line in open(TRAFFIC_FILE):
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("combine_cu_sha256_16") == src_hash:
+            return int(float(kv["dram_bytes_per_launch"]))
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.lines = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                    "-lms", "50"]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t_start, t_end):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                sm = float(f[2].split()[0])
+                smax = float(f[3].split()[0])
+            except (ValueError, IndexError):
+                continue
+            reasons = [n for n, v in zip(("hw_slowdown", "hw_thermal_slowdown",
+                                          "sw_thermal_slowdown", "sw_power_cap"), f[6:10])
+                       if v.lower().startswith("active")]
+            rows.append((ts, sm, smax, reasons))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inwin = [r for r in rows if t_start - 0.05 <= r[0] <= t_end + 0.05]
+        window = "timed"
+        if not inwin:
+            inwin, window = rows, "warmup+timed"
+        reasons = sorted({x for r in inwin for x in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in inwin),
+                "sm_max_mhz": max(r[2] for r in inwin), "reasons": reasons,
+                "samples": len(inwin), "window": window}
+
+
+# ------------------------------------------------------------ CPU baseline
+def oracle_tokens_per_s(w, idx, wts, x, y_host, n_tokens):
+    """Run the oracle's layout + dispatch + combine on the first n_tokens tokens."""
+    import oracle
+    orc = oracle.default()
+    sub_idx = np.ascontiguousarray(idx[:n_tokens])
+    sub_w = np.ascontiguousarray(wts[:n_tokens])
+    sub_x = np.ascontiguousarray(x[:n_tokens])
+    t0 = time.perf_counter()
+    L = orc.layout(sub_idx, w.E, w.layout, align=w.align, cap=w.cap, R=w.R)
+    orc.dispatch(sub_x, L["dst_row"], L["rows"], w.quant)
+    need = max(L["rows"], 1)
+    orc.combine(y_host[:need], sub_w, L["dst_row"], w.H)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt
+
+
+def y_host_rows(w, rows):
+    # oracle-side expert outputs: seeded bf16 N(0,1) rows (host generator)
+    import torch
+    return workloads.make_expert_outputs(rows, w.H, seed=7, device="cpu").view(
+        torch.int16).numpy().view(np.uint16)
+
+
+def cpu_baseline(w, idx, wts, x, target_s=10.0):
+    y_host = y_host_rows(w, 256 * w.K + w.E * w.align)
+    rate, dt = oracle_tokens_per_s(w, idx, wts, x, y_host, 256)
+    n = int(min(w.T, max(256, rate * target_s)))
+    if n > 256:
+        y_host = y_host_rows(w, n * w.K + w.E * w.align)
+        rate, dt = oracle_tokens_per_s(w, idx, wts, x, y_host, n)
+    return {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} of {w.T} tokens of {w.name}, one pass of layout + dispatch "
+                      f"+ combine, single-threaded C oracle ({dt:.1f} s)"}
+
+
+# ---------------------------------------------------------------- reference
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    idx, wts, x = workloads.make_inputs(w)
+    y_host = y_host_rows(w, 256 * w.K + w.E * w.align)
+    rate, _ = oracle_tokens_per_s(w, idx, wts, x, y_host, 256)
+    budget = 60.0  # seconds for the whole --warmup + --steps run
+    n = int(max(16, min(w.T, rate * budget / max(1, args.steps + args.warmup))))
+    y_host = y_host_rows(w, n * w.K + w.E * w.align)
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(w, idx, wts, x, y_host, n)
+    total_dt = 0.0
+    for _ in range(args.steps):
+        _, dt = oracle_tokens_per_s(w, idx, wts, x, y_host, n)
+        total_dt += dt
+    value = n * args.steps / total_dt
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 dispatch, fp32-accumulate combine",
+            "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "K": w.K,
+                       "layout": "contig align 128", "quant": w.quant,
+                       "sample_tokens_per_step": n},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"first {n} of {w.T} tokens per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- ours
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from combine_expert_histogram_gb300 import binding as ep
+    from combine_expert_histogram_gb300 import build as epbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if not epbuild.up_to_date() and rank == 0:
+        epbuild.build()
+    if world > 1:
+        dist.barrier()
+
+    # inputs (seeded; each replica gets its own batch)
+    wr = w.with_(seed=w.seed + rank)
+    idx, wts, x = workloads.make_inputs(wr)
+    idx_d = torch.from_numpy(idx).to(dev)
+    w_d = torch.from_numpy(wts).to(dev)
+    x_d = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    L = ep.new_layout(w.T, w.K, w.E, w.layout, align=w.align, capacity=w.cap, num_ranks=w.R,
+                      device=dev)
+    rows = L.rows_capacity
+    out_rows = torch.empty((rows, w.H), device=dev,
+                           dtype=torch.bfloat16 if w.quant == "none" else torch.uint8)
+    out_scales = None
+    if w.quant != "none":
+        out_scales = torch.empty((rows, ep.ep_scale_cols(w.H, w.quant)), device=dev,
+                                 dtype=torch.float32 if w.quant == "fp8_f32" else torch.int32)
+    y = workloads.make_expert_outputs(rows, w.H, seed=7 + rank, device=dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    n_layout_kernels = 2 if ep.ep_layout_workspace_bytes(L) > 0 else 1
+    launches_per_step = n_layout_kernels + 2
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ep.ep_layout(idx_d, w.E, out=L, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ep.ep_dispatch(L, x_d, w.quant, out_rows=out_rows, out_scales=out_scales, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        ep.ep_combine(L, y, w_d, out=out, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    L.check_status()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+                    for e in evs])
+    lay_ms, disp_ms, comb_ms = seg.mean(axis=0)
+    ab = algorithmic_bytes(w)
+    peak, peak_src = peak_hbm()
+    kern = {}
+    for name, ms in (("layout", lay_ms), ("dispatch", disp_ms), ("combine", comb_ms)):
+        gbs = ab[name] / (ms * 1e-3) / 1e9
+        kern[name] = {"us": round(ms * 1e3, 2), "algorithmic_bytes": ab[name],
+                      "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if rank == 0 and not args.skip_e2e:
+        e2e = measure_e2e(ep, w, L, idx, wts, x, y, out_rows, out_scales, dev, stream, args)
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    tokens = w.T * args.steps * world
+    value = tokens / (elapsed_ms * 1e-3)
+    dom = max(("dispatch", "combine"), key=lambda k: kern[k]["us"])
+    traffic = combine_traffic() if dom == "combine" else None
+    achieved = kern[dom]["GB/s"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3 dispatch (fp32 scales), bf16 in / fp32-accumulate combine",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "K": w.K,
+                   "routing": "grouped sigmoid + N(0,0.1) bias, 8 groups / top-4",
+                   "layout": "expert-contiguous, 128-row aligned", "quant": w.quant,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": (f"inputs larger than L2: x {x_d.numel() * 2 / 1e6:.0f} MB, "
+                          f"y {y.numel() * 2 / 1e9:.2f} GB, rows {out_rows.numel() / 1e9:.2f} GB "
+                          f"(L2 129 MB); no flush")},
+        "step_gbs": round(sum(ab.values()) * args.steps * world / (elapsed_ms * 1e-3) / 1e9, 1),
+        "kernels": kern,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ab[dom]},
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if sampler:
+        line["clocks"] = sampler.summary(t_wall0, t_wall1)
+    if e2e:
+        line["e2e"] = e2e
+    if not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, idx, wts, x)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def measure_e2e(ep, w, L, idx, wts, x, y_dev, out_rows, out_scales, dev, stream, args):
+    """Same metric through the public API with inputs in pinned host memory:
+    every step copies x, topk_idx, topk_w and the expert outputs y host->device,
+    runs layout + dispatch + combine and copies the combined output (and the
+    expert histogram) back."""
+    import torch
+    pin = dict(pin_memory=True)
+    h_idx = torch.from_numpy(idx).pin_memory()
+    h_w = torch.from_numpy(wts).pin_memory()
+    h_x = torch.from_numpy(x.view(np.int16)).pin_memory()
+    h_y = torch.empty(y_dev.shape, dtype=torch.int16, **pin)
+    h_y.copy_(y_dev.view(torch.int16))
+    h_out = torch.empty((w.T, w.H), dtype=torch.int16, **pin)
+    h_cnt = torch.empty(w.E, dtype=torch.int32, **pin)
+    d_idx = torch.empty_like(h_idx, device=dev)
+    d_w = torch.empty_like(h_w, device=dev)
+    d_x = torch.empty(h_x.shape, dtype=torch.int16, device=dev)
+    d_y = torch.empty(h_y.shape, dtype=torch.int16, device=dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_idx, h_w, h_x, h_y))
+    d2h = h_out.numel() * 2 + h_cnt.numel() * 4
+
+    def step():
+        with torch.cuda.stream(stream):
+            d_idx.copy_(h_idx, non_blocking=True)
+            d_w.copy_(h_w, non_blocking=True)
+            d_x.copy_(h_x, non_blocking=True)
+            d_y.copy_(h_y, non_blocking=True)
+            ep.ep_layout(d_idx, w.E, out=L, stream=stream)
+            ep.ep_dispatch(L, d_x.view(torch.bfloat16), w.quant, out_rows=out_rows,
+                           out_scales=out_scales, stream=stream)
+            ep.ep_combine(L, d_y.view(torch.bfloat16), d_w, out=out, stream=stream)
+            h_out.copy_(out.view(torch.int16), non_blocking=True)
+            h_cnt.copy_(L.expert_count, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 20))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"value": w.T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": n}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
+    ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer e2e leg")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T (small cases for profiling; not a bench line)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = workloads.CONFIGS[args.workload]
+    if args.tokens:
+        w = w.with_(T=args.tokens, name=f"{w.name}_T{args.tokens}")
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

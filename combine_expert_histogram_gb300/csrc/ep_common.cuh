@@ -1,0 +1,112 @@
+// Shared device helpers and internal launcher declarations for the sm_103a
+// dispatch / combine library.  The public C ABI is include/ep.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ep.h"
+
+namespace ep {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// Record a data-dependent error: the status word keeps the largest code seen.
+__device__ __forceinline__ void raise_status(int32_t *status, int code) {
+    atomicMax(status, code);
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Streaming 16-byte load of data read exactly once (no L1 allocation).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Two packed bf16 -> two fp32 (exact: bf16 is the top half of binary32).
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// Exclusive scan over n <= 2*NT values produced by value(i), by one CTA of NT
+// threads.  out[i] = value(0) + ... + value(i-1) for i in [0, n], out[n] = total.
+// `tmp` holds NT/32 ints of shared memory.  Must be reached by every thread.
+template <int NT, typename F>
+__device__ __forceinline__ void block_exclusive_scan(int n, F value, int32_t *out,
+                                                     int32_t *tmp) {
+    static_assert(NT % 32 == 0 && NT / 32 <= 32, "one warp scans the warp totals");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int i0 = 2 * threadIdx.x, i1 = i0 + 1;
+    const int v0 = i0 < n ? value(i0) : 0;
+    const int v1 = i1 < n ? value(i1) : 0;
+    const int s = v0 + v1;
+    int incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int o = __shfl_up_sync(kFullMask, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) tmp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = lane < NT / 32 ? tmp[lane] : 0;
+        int wi = wv;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int o = __shfl_up_sync(kFullMask, wi, d);
+            if (lane >= d) wi += o;
+        }
+        if (lane < NT / 32) tmp[lane] = wi - wv;
+    }
+    __syncthreads();
+    const int excl = tmp[warp] + incl - s;
+    if (i0 < n) out[i0] = excl;
+    if (i1 < n) out[i1] = excl + v0;
+    if (i0 == n - 1) out[n] = excl + v0;
+    if (i1 == n - 1) out[n] = excl + s;
+    if (n == 0 && threadIdx.x == 0) out[0] = 0;
+    __syncthreads();
+}
+
+// Per-device properties, cached on first use (host side).
+int sm_count();
+
+// Internal launchers (one translation unit each).  They assume arguments were
+// validated by the C ABI layer in abi.cu.
+struct LayoutPlan {
+    int tiles;        // tiles of topk_idx entries (CTAs that assign slots)
+    int tile;         // entries per tile, a multiple of 512
+    int grid;         // CTAs of the assign kernel (>= tiles; extra CTAs fill padding)
+    size_t smem;      // dynamic shared memory of the assign kernel
+    size_t ws_bytes;  // scratch: tiles x E int32 per-tile histograms (0 when tiles == 1)
+};
+LayoutPlan layout_plan(const ep_layout_t &L);
+cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t *workspace,
+                          cudaStream_t stream);
+
+cudaError_t launch_dispatch(const ep_layout_t &L, const void *x, int H, ep_quant_t quant,
+                            void *out_rows, void *out_scales, const float *topk_w,
+                            float *row_w, cudaStream_t stream);
+
+cudaError_t launch_combine(const ep_layout_t &L, const void *y, int H, const float *topk_w,
+                           void *out, cudaStream_t stream);
+
+cudaError_t launch_masked_repack(const ep_layout_t &L, const void *rows,
+                                 const void *row_scales, int H, ep_quant_t quant, int cap,
+                                 void *slab, void *slab_scales, int32_t *masked_m,
+                                 cudaStream_t stream);
+
+}  // namespace ep

@@ -1,0 +1,84 @@
+// ep_masked_repack kernel: copy a contiguous layout's expert segments into the
+// masked decode slab [E, cap, H] (the "masked-slab repack kernels" of SGLang
+// PR "[Feature] Add DeepEPv2 (ElasticBuffer) MoE A2A backend", section
+// "Implementation", for both fp32 and packed UE8M0 scales).
+//
+// Byte copy, HBM-bound.  Every CTA scans m_e = min(count[e], cap) into shared
+// memory, then its warps walk the flat list of valid rows grid-stride; a
+// binary search over the prefix finds (expert, slot) of a flat row.  One warp
+// copies one row with 16-byte vectors and its scale words with 4-byte words.
+#include "ep_common.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kThreads = 512;
+
+__global__ void __launch_bounds__(kThreads)
+    repack_kernel(const uint8_t *__restrict__ rows, const uint8_t *__restrict__ row_scales,
+                  int row_bytes, int scale_bytes, const int32_t *__restrict__ offset,
+                  const int32_t *__restrict__ count, int E, int cap,
+                  uint8_t *__restrict__ slab, uint8_t *__restrict__ slab_scales,
+                  int32_t *__restrict__ masked_m, int32_t *__restrict__ status) {
+    extern __shared__ int32_t pre[];  // [E+1]
+    __shared__ int32_t scan_tmp[kThreads / 32];
+    block_exclusive_scan<kThreads>(
+        E, [&](int e) { return min(__ldg(count + e), cap); }, pre, scan_tmp);
+
+    if (blockIdx.x == 0) {
+        for (int e = threadIdx.x; e < E; e += kThreads) {
+            const int c = __ldg(count + e);
+            masked_m[e] = min(c, cap);
+            if (c > cap) raise_status(status, EP_ERR_CAPACITY);
+        }
+    }
+
+    const int lane = threadIdx.x & 31;
+    const int total = pre[E];
+    const int warps = gridDim.x * (kThreads / 32);
+    for (int r = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < total; r += warps) {
+        int lo = 0, hi = E;  // pre[lo] <= r < pre[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pre[mid] <= r) lo = mid; else hi = mid;
+        }
+        const int s = r - pre[lo];
+        const size_t src = (size_t)__ldg(offset + lo) + s;
+        const size_t dst = (size_t)lo * cap + s;
+        const uint8_t *sp = rows + src * row_bytes;
+        uint8_t *dp = slab + dst * row_bytes;
+        for (int b = lane * 16; b < row_bytes; b += 32 * 16) st_v4(dp + b, ld_stream(sp + b));
+        if (scale_bytes) {
+            const uint32_t *ss = reinterpret_cast<const uint32_t *>(row_scales + src * scale_bytes);
+            uint32_t *ds = reinterpret_cast<uint32_t *>(slab_scales + dst * scale_bytes);
+            for (int b = lane; b < scale_bytes / 4; b += 32) ds[b] = __ldg(ss + b);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_masked_repack(const ep_layout_t &L, const void *rows,
+                                 const void *row_scales, int H, ep_quant_t quant, int cap,
+                                 void *slab, void *slab_scales, int32_t *masked_m,
+                                 cudaStream_t stream) {
+    const int E = L.num_experts;
+    const int row_bytes = quant == EP_QUANT_NONE ? 2 * H : H;
+    const int G = H / 128;
+    const int scale_bytes = quant == EP_QUANT_FP8_F32 ? 4 * G
+                            : quant == EP_QUANT_FP8_UE8M0 ? 4 * ((G + 3) / 4) : 0;
+    // Enough warps to keep HBM busy: the valid rows number at most T*K.
+    const long long rows_max = (long long)L.num_tokens * L.num_topk;
+    long long blocks = (rows_max + kThreads / 32 - 1) / (kThreads / 32);
+    const long long limit = 4LL * sm_count();
+    if (blocks > limit) blocks = limit;
+    if (blocks < 1) blocks = 1;
+    const size_t smem = sizeof(int32_t) * (size_t)(E + 1);
+    repack_kernel<<<(unsigned)blocks, kThreads, smem, stream>>>(
+        static_cast<const uint8_t *>(rows), static_cast<const uint8_t *>(row_scales), row_bytes,
+        scale_bytes, L.expert_offset, L.expert_count, E, cap, static_cast<uint8_t *>(slab),
+        static_cast<uint8_t *>(slab_scales), masked_m, L.status);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

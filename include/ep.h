@@ -1,0 +1,234 @@
+/*
+ * ep.h -- MoE token dispatch and combine on one GPU (GB300, sm_103a): C ABI.
+ *
+ * The hot path of expert-parallel MoE layers, on one device whose HBM holds
+ * every expert: logical expert-parallel ranks are only partitions of the
+ * expert set.  Four operations:
+ *
+ *   ep_layout         top-k router output -> per-expert layout: expert
+ *                     histogram, padded exclusive scan, stable slots.
+ *   ep_dispatch       scatter token rows into that layout, optionally fused
+ *                     with dynamic 1x128 FP8-E4M3 quantisation.
+ *   ep_combine        top-k weighted reduction of expert outputs back to
+ *                     token order.
+ *   ep_masked_repack  contiguous expert segments -> masked [E, cap, H] slab.
+ *
+ * Sources (the pages describe a library integration, not kernels):
+ *   [PR-24443]  SGLang PR "moe: add DeepEP V2 ElasticBuffer support to MoE
+ *               token dispatcher", section "Motivation" (V2 dispatch infers
+ *               the layout from topk_idx; per-expert receive counts live on
+ *               the handle; combine reuses the dispatch handle) and the review
+ *               thread on num_topk ("lots of kNumTopk <= 32 restrictions"),
+ *               and its commit "num_max_tokens_per_rank sizing" (dispatch
+ *               hard-asserts num_tokens <= num_max_tokens_per_rank).
+ *   [PR-35634]  SGLang PR "[Feature] Add DeepEPv2 (ElasticBuffer) MoE A2A
+ *               backend": "Supported scope" (decode uses the expanded masked
+ *               layout, extend/prefill the contiguous layout; dynamic
+ *               blockwise FP8), "Implementation" (masked-slab repack kernels;
+ *               Hopper FP32 scales and Blackwell packed UE8M0 scales;
+ *               single-use handles), "Capacity and fail-fast behavior".
+ *   [DISC-26563] SGLang discussion "deepep v2 support?": the expert-format
+ *               gate (128x128 blockwise FP8 with dynamic activation scaling,
+ *               or unquantised BF16).
+ *   [VLLM-EP]   vLLM tools/ep_kernels commit adding the deepep_v2 backend:
+ *               do_expand=True gives a per-expert-contiguous layout, with
+ *               weighted reduction in combine; FP8 block-quantised dispatch.
+ *
+ * Conventions for every call:
+ *   - All array arguments are DEVICE pointers owned by the caller; the library
+ *     allocates nothing, keeps no global state and never synchronises the host.
+ *     Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and completes asynchronously.
+ *   - Host-detectable errors (bad shapes, NULL or misaligned pointers, too many
+ *     tokens) are returned synchronously and nothing is launched.  A failed
+ *     launch returns EP_ERR_CUDA.
+ *   - Data-dependent errors are raised on the device into the layout's status
+ *     word as the maximum of the codes seen (no trap, no assert, no
+ *     out-of-bounds write): EP_ERR_BAD_EXPERT_ID for an id outside [-1, E),
+ *     EP_ERR_CAPACITY for a masked expert receiving more than `capacity` rows.
+ *     Read it back after the stream completes.
+ *   - bf16 means IEEE binary32's upper 16 bits; FP8 means E4M3FN (OCP OFP8).
+ */
+#ifndef EP_H_
+#define EP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ep_stream_t; /* identical to cudaStream_t */
+
+typedef enum ep_status {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,   /* bad shape, enum, NULL or misaligned pointer    */
+    EP_ERR_CAPACITY = 2,      /* too many tokens / rows for the reserved space  */
+    EP_ERR_BAD_EXPERT_ID = 3, /* device-side only: id outside [-1, E)          */
+    EP_ERR_CUDA = 4,          /* a CUDA launch failed                           */
+    EP_ERR_UNSUPPORTED = 5    /* valid request this build does not implement    */
+} ep_status_t;
+
+typedef enum ep_layout_kind {
+    EP_LAYOUT_CONTIG = 0, /* expanded per-expert-contiguous rows (prefill)  */
+    EP_LAYOUT_MASKED = 1  /* [E, capacity, H] slab + per-expert counts (decode) */
+} ep_layout_kind_t;
+
+typedef enum ep_quant {
+    EP_QUANT_NONE = 0,     /* bf16 rows                                           */
+    EP_QUANT_FP8_F32 = 1,  /* E4M3 rows + fp32 scale per 1x128 group  [rows, H/128]  */
+    EP_QUANT_FP8_UE8M0 = 2 /* E4M3 rows + UE8M0 exponent per group, 4 per int32 word
+                              [rows, ceil(H/512)]                                   */
+} ep_quant_t;
+
+#define EP_MAX_TOPK 32     /* [PR-24443] review: kNumTopk <= 32 */
+#define EP_MAX_EXPERTS 1024
+#define EP_MAX_ALIGN 128
+
+/*
+ * The layout ("handle"): shape plus caller-owned device arrays.  ep_layout()
+ * fills the arrays; ep_dispatch() and ep_combine() read them, so combine
+ * reuses exactly the dispatch handle ([PR-24443] "Motivation"; [PR-35634]
+ * "Implementation").  T = num_tokens, K = num_topk, E = num_experts.
+ *
+ * Row space: contiguous -> rows = expert_offset[E] (at most ep_rows_capacity);
+ *            masked     -> rows = E * capacity, expert e owns rows
+ *                          [e*capacity, (e+1)*capacity).
+ */
+typedef struct ep_layout {
+    /* shape, set by the caller */
+    int32_t num_tokens;  /* T >= 0                                                 */
+    int32_t num_topk;    /* K in [1, EP_MAX_TOPK]                                   */
+    int32_t num_experts; /* E in [1, EP_MAX_EXPERTS]                                */
+    int32_t num_ranks;   /* R >= 1 logical ranks, R divides E; rank r owns experts
+                            [r*E/R, (r+1)*E/R)                                      */
+    int32_t kind;        /* ep_layout_kind_t                                        */
+    int32_t align;       /* contiguous: segment alignment in rows, a power of two in
+                            [1, EP_MAX_ALIGN]; masked: ignored                      */
+    int32_t capacity;    /* masked: slots per expert, >= 1; contiguous: ignored      */
+    int32_t max_tokens;  /* reserved token capacity: T > max_tokens is rejected with
+                            EP_ERR_CAPACITY before any launch ([PR-24443] commit
+                            "num_max_tokens_per_rank sizing"; [PR-35634] "Capacity
+                            and fail-fast behavior").  0 = no limit.               */
+    /* device arrays, caller-owned, int32 */
+    int32_t *dst_row;       /* [T*K] row of entry (t,k) = t*K+k; -1 if not placed   */
+    int32_t *row_src;       /* [rows] entry t*K+k that fills each row, -1 for padding
+                               and empty slots; may be NULL                        */
+    int32_t *expert_count;  /* [E] expert histogram (rows requested per expert)     */
+    int32_t *expert_offset; /* [E+1] first row of each expert; [E] = rows            */
+    int32_t *rank_rows;     /* [R] rows requested per logical rank; may be NULL       */
+    int32_t *status;        /* [1] device status word, reset by ep_layout            */
+} ep_layout_t;
+
+/* Human-readable name of a status code (static storage). */
+const char *ep_status_str(ep_status_t status);
+
+/* Rows a row buffer / row_src must hold: contiguous T*K + min(E, T*K)*(align-1)
+ * (the worst case of the padded scan), masked E*capacity.  -1 on a bad layout. */
+int64_t ep_rows_capacity(const ep_layout_t *layout);
+
+/* 32-bit scale words per row: H/128 (fp32 scales), ceil(H/512) (packed UE8M0),
+ * 0 (bf16); -1 if `hidden` is not valid for `quant`. */
+int64_t ep_scale_cols(int32_t hidden, ep_quant_t quant);
+
+/* Bytes of device scratch ep_layout() needs for this shape (may be 0).  The
+ * scratch holds per-tile expert histograms between the two layout kernels. */
+size_t ep_layout_workspace_bytes(const ep_layout_t *layout);
+
+/*
+ * ep_layout -- expert histogram, padded exclusive scan, stable slot assignment
+ * ([PR-24443] "Motivation": V2 dispatch infers the layout from topk_idx and
+ * returns the per-expert receive counts; [PR-35634] "Supported scope" /
+ * [VLLM-EP]: per-expert-contiguous and masked layouts).
+ *
+ *   topk_idx   device int32 [T, K], row-major; -1 = not routed.
+ *   layout     shape + output arrays (see ep_layout_t); status is reset to 0.
+ *   workspace  device scratch of at least ep_layout_workspace_bytes() bytes
+ *              (NULL allowed when that is 0), 4-byte aligned; clobbered.
+ *
+ * Computes, for every entry i = t*K+k with e = topk_idx[i] in [0, E):
+ *   expert_count[e]  = #entries with id e
+ *   expert_offset    = contiguous: exclusive scan of roundup(count, align);
+ *                      masked: e*capacity
+ *   slot(i)          = #entries j < i with the same id (ascending token, then k)
+ *   dst_row[i]       = expert_offset[e] + slot(i); -1 for -1 ids, bad ids, and
+ *                      masked slots >= capacity (EP_ERR_CAPACITY raised)
+ *   row_src[dst_row[i]] = i; every other row of the row space = -1
+ *   rank_rows[r]     = sum of expert_count over rank r's experts
+ */
+ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *layout, void *workspace,
+                      size_t workspace_bytes, ep_stream_t stream);
+
+/*
+ * ep_dispatch -- scatter token rows into the layout, fused with dynamic 1x128
+ * FP8-E4M3 quantisation ([PR-35634] "Supported scope", "Implementation";
+ * [DISC-26563] 128x128 blockwise FP8 with dynamic activation scaling;
+ * [VLLM-EP] FP8 block-quantised dispatch).
+ *
+ *   x           device bf16 [T, hidden], 16-byte aligned.
+ *   hidden      H; a multiple of 128 for FP8, of 8 for bf16.
+ *   out_rows    device [rows, H]: bf16 (EP_QUANT_NONE) or E4M3 bytes; 16-byte
+ *               aligned.  Only rows named by dst_row are written; padding rows
+ *               and empty slots are left untouched.
+ *   out_scales  device [rows, ep_scale_cols(H, quant)] fp32 or int32, 4-byte
+ *               aligned; NULL for EP_QUANT_NONE.
+ *   topk_w      optional device fp32 [T, K]; with row_w (device fp32 [rows]),
+ *               row_w[dst_row[i]] = topk_w[i]. Both NULL to skip.
+ *
+ * For each token t and 128-wide group g of x[t]:
+ *   amax  = max |x|;  s = max(amax, 1e-4) / 448   (fp32, IEEE division)
+ *   FP8_F32:   q = E4M3_rn_satfinite(x / s), scale = s
+ *   FP8_UE8M0: s rounded up to 2^(e-127) (e = biased exponent of s, plus one
+ *              when s is not a power of two); q = E4M3_rn_satfinite(x * 2^(127-e));
+ *              byte g%4 of int32 word g/4 (little-endian) = e; unused bytes 127.
+ * and the same bytes are written to every row dst_row[t*K+k] >= 0.
+ */
+ep_status_t ep_dispatch(const ep_layout_t *layout, const void *x, int32_t hidden,
+                        ep_quant_t quant, void *out_rows, void *out_scales,
+                        const float *topk_w, float *row_w, ep_stream_t stream);
+
+/*
+ * ep_combine -- top-k weighted reduction back to token order ([VLLM-EP]
+ * "weighted reduction in combine"; combine reuses the dispatch handle,
+ * [PR-24443] "Motivation").  The reduction is applied exactly once.
+ *
+ *   y        device bf16 expert outputs in the layout's row space [rows, H]
+ *            (masked: [E, capacity, H]), 16-byte aligned.
+ *   topk_w   device fp32 [T, K].
+ *   out      device bf16 [T, H], 16-byte aligned; every element is written.
+ *
+ *   out[t,h] = bf16_rn( sum over k = 0..K-1 with dst_row[t*K+k] >= 0 of
+ *                       topk_w[t,k] * y[dst_row[t*K+k], h] )
+ * accumulated in fp32 in ascending k, each product and sum rounded separately
+ * (no fused multiply-add); a token with no placed entry gets +0.
+ */
+ep_status_t ep_combine(const ep_layout_t *layout, const void *y, int32_t hidden,
+                       const float *topk_w, void *out, ep_stream_t stream);
+
+/*
+ * ep_masked_repack -- copy a contiguous layout's expert segments into the
+ * masked decode slab ([PR-35634] "Implementation": masked-slab repack kernels
+ * with Hopper FP32 and Blackwell packed UE8M0 scales).
+ *
+ *   layout       a CONTIGUOUS layout already filled by ep_layout().
+ *   rows         device [rows, H] bf16 or E4M3 (as written by ep_dispatch).
+ *   row_scales   device [rows, ep_scale_cols] or NULL for EP_QUANT_NONE.
+ *   capacity     slab slots per expert, >= 1.
+ *   slab         device [E, capacity, H]; slab_scales [E, capacity, cols].
+ *   masked_m     device int32 [E] = min(expert_count[e], capacity).
+ *
+ *   slab[e, s] = rows[expert_offset[e] + s] for s < masked_m[e]; other slab rows
+ *   are untouched.  expert_count[e] > capacity raises EP_ERR_CAPACITY into the
+ *   layout's status word.
+ */
+ep_status_t ep_masked_repack(const ep_layout_t *layout, const void *rows,
+                             const void *row_scales, int32_t hidden, ep_quant_t quant,
+                             int32_t capacity, void *slab, void *slab_scales,
+                             int32_t *masked_m, ep_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_H_ */

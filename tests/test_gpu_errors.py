@@ -1,0 +1,93 @@
+"""Error paths on the GPU: data-dependent errors land in the status word, never
+as a trap, a hang or an out-of-bounds write (guard bands around every output
+are checked).  Host-detectable errors return before any launch."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_expert_histogram_gb300 import binding as ep
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+GUARD = 4096
+PAT = 0x5A5A5A5A - (1 << 32)  # int32 pattern
+
+
+def _guarded(n, dtype=torch.int32):
+    buf = torch.full((n + 2 * GUARD,), PAT, dtype=torch.int32, device="cuda")
+    return buf, buf[GUARD:GUARD + n]
+
+
+def _guards_intact(buf, n):
+    return bool((buf[:GUARD] == PAT).all()) and bool((buf[GUARD + n:] == PAT).all())
+
+
+@pytest.mark.parametrize("T", [50, 3000])  # one tile and several tiles
+def test_bad_expert_ids_raise_status_without_stray_writes(T):
+    E, K = 16, 4
+    rng = np.random.default_rng(0)
+    idx = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    idx[3, 1] = E
+    idx[7, 0] = -5
+    idx[T - 1, 3] = 1 << 30
+    L = ep.new_layout(T, K, E, "contig", align=8)
+    rows = L.rows_capacity
+    rs_buf, L.row_src = _guarded(rows)
+    dr_buf, L.dst_row = _guarded(T * K)
+    ep.ep_layout(torch.from_numpy(idx).cuda(), E, out=L)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == ep.EP_ERR_BAD_EXPERT_ID
+    with pytest.raises(ep.EPError):
+        L.check_status()
+    ref = oracle.default().layout(idx, E, "contig", align=8)
+    assert ref["status"] == 3
+    assert np.array_equal(L.dst_row.cpu().numpy().reshape(T, K), ref["dst_row"])
+    assert np.array_equal(L.row_src.cpu().numpy()[:ref["rows"]], ref["row_src"])
+    assert _guards_intact(rs_buf, rows) and _guards_intact(dr_buf, T * K)
+
+
+@pytest.mark.parametrize("T", [40, 4000])
+def test_masked_capacity_overflow(T):
+    E, K, cap = 8, 4, 9
+    rng = np.random.default_rng(1)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    L = ep.new_layout(T, K, E, "masked", capacity=cap)
+    rows = E * cap
+    rs_buf, L.row_src = _guarded(rows)
+    ep.ep_layout(torch.from_numpy(idx).cuda(), E, kind="masked", capacity=cap, out=L)
+    x = torch.randn(T, 256, device="cuda").to(torch.bfloat16)
+    out_buf = torch.full(((rows + 8) * 256,), 0x5A, dtype=torch.uint8, device="cuda")
+    out_rows = out_buf[4 * 256:(rows + 4) * 256].view(rows, 256)
+    sc = torch.zeros(rows, 2, dtype=torch.float32, device="cuda")
+    ep.ep_dispatch(L, x, "fp8_f32", out_rows=out_rows, out_scales=sc)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == ep.EP_ERR_CAPACITY
+    ref = oracle.default().layout(idx, E, "masked", cap=cap)
+    assert ref["status"] == 2
+    assert np.array_equal(L.dst_row.cpu().numpy().reshape(T, K), ref["dst_row"])
+    assert np.array_equal(L.expert_count.cpu().numpy(), ref["count"])
+    assert _guards_intact(rs_buf, rows)
+    assert bool((out_buf[:4 * 256] == 0x5A).all()) and bool((out_buf[(rows + 4) * 256:] == 0x5A).all())
+
+
+def test_token_capacity_is_checked_before_launch():
+    idx = torch.zeros(200, 8, dtype=torch.int32, device="cuda")
+    with pytest.raises(ep.EPError) as ei:
+        ep.ep_layout(idx, 16, max_tokens=128)
+    assert ei.value.code == ep.EP_ERR_CAPACITY
+
+
+def test_status_resets_on_next_layout():
+    E = 4
+    bad = torch.tensor([[0, 9]], dtype=torch.int32, device="cuda")
+    L = ep.ep_layout(bad, E, align=4)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == ep.EP_ERR_BAD_EXPERT_ID
+    good = torch.tensor([[0, 3]], dtype=torch.int32, device="cuda")
+    ep.ep_layout(good, E, align=4, out=L)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0

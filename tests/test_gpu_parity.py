@@ -1,0 +1,192 @@
+"""CUDA path vs the CPU oracle, through the C ABI (needs a GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import gpu_harness as gh
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # the whole module needs a device
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from combine_expert_histogram_gb300 import build as b
+    b.build()
+
+
+# The five workloads at full size; the two largest compare sampled tokens
+# (every layout entry is still checked).
+FULL = {"tiny": None, "qwen3_30b_a3b_decode": None, "dsv3_decode": None,
+        "dsv3_prefill": 384, "skewed_zipf": 1024}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_workload_parity(name):
+    w = workloads.CONFIGS[name]
+    case = gh.make_case(w)
+    g = gh.run_gpu(w, case)
+    ref = gh.check_layout(w, case, g)
+    assert ref["status"] == 0
+    gh.check_dispatch(w, case, g, ref, sample_tokens=FULL[name])
+    frac = gh.check_combine(w, case, g, ref, sample_tokens=FULL[name])
+    assert frac == 1.0, f"combine within 1 ulp but only {frac:.6f} bit-exact"
+
+
+# Mid-size cases: several layout tiles with a ragged tail, hidden sizes whose
+# UE8M0 words are partly padding, alignment 1, one hot expert, -1 ids.
+MID = [
+    workloads.Workload("ragged_fp8_ue8m0", T=3001, H=640, E=64, K=8, routing="softmax",
+                       layout="contig", quant="fp8_ue8m0", align=128, R=4, seed=3),
+    workloads.Workload("ragged_fp8_f32_masked", T=2049, H=384, E=96, K=6, routing="softmax",
+                       layout="masked", quant="fp8_f32", cap=2049, seed=4),
+    workloads.Workload("ragged_bf16_align1", T=1500, H=264, E=40, K=7, routing="zipf",
+                       layout="contig", quant="none", align=1, R=8, seed=5),
+    workloads.Workload("k32", T=600, H=1024, E=256, K=32, routing="softmax",
+                       layout="contig", quant="fp8_f32", align=64, seed=6),
+    workloads.Workload("k1_e1", T=777, H=256, E=1, K=1, routing="softmax",
+                       layout="contig", quant="fp8_ue8m0", align=128, seed=7),
+    workloads.Workload("e1024_masked", T=300, H=512, E=1024, K=4, routing="softmax",
+                       layout="masked", quant="fp8_ue8m0", cap=16, R=16, seed=8),
+    workloads.Workload("h128", T=5000, H=128, E=32, K=2, routing="softmax",
+                       layout="contig", quant="fp8_f32", align=32, seed=9),
+]
+
+
+@pytest.mark.parametrize("w", MID, ids=lambda w: w.name)
+def test_mid_parity(w):
+    case = gh.make_case(w)
+    g = gh.run_gpu(w, case)
+    ref = gh.check_layout(w, case, g)
+    gh.check_dispatch(w, case, g, ref)
+    assert gh.check_combine(w, case, g, ref) == 1.0
+
+
+def _custom_case(w, idx, wts=None):
+    rng = np.random.default_rng(11)
+    x = workloads.make_x(w, rng)
+    if wts is None:
+        wts = rng.random(idx.shape).astype(np.float32)
+    return dict(idx=idx, w=wts, x=x, idx_d=torch.from_numpy(idx).cuda(),
+                w_d=torch.from_numpy(wts).cuda(),
+                x_d=torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
+
+
+@pytest.mark.parametrize("layout", ["contig", "masked"])
+def test_single_hot_expert_and_unrouted(layout):
+    """Every token on expert 3 plus -1 entries; spans several layout tiles."""
+    T, K, E = 5000, 4, 16
+    w = workloads.Workload("hot", T=T, H=512, E=E, K=K, routing="softmax", layout=layout,
+                           quant="fp8_f32", align=128, cap=T + 5)
+    idx = np.full((T, K), -1, dtype=np.int32)
+    idx[:, 0] = 3
+    idx[::3, 2] = 7
+    case = _custom_case(w, idx)
+    g = gh.run_gpu(w, case)
+    ref = gh.check_layout(w, case, g)
+    gh.check_dispatch(w, case, g, ref)
+    assert gh.check_combine(w, case, g, ref) == 1.0
+
+
+def test_repeated_expert_within_token():
+    """A token may name one expert twice: slots follow ascending k."""
+    T, K, E = 2100, 3, 5
+    w = workloads.Workload("rep", T=T, H=256, E=E, K=K, routing="softmax", layout="contig",
+                           quant="none", align=4)
+    idx = np.random.default_rng(2).integers(0, E, size=(T, K)).astype(np.int32)
+    case = _custom_case(w, idx)
+    g = gh.run_gpu(w, case)
+    ref = gh.check_layout(w, case, g)
+    gh.check_dispatch(w, case, g, ref)
+    assert gh.check_combine(w, case, g, ref) == 1.0
+
+
+@pytest.mark.parametrize("T", [0, 1])
+def test_tiny_token_counts(T):
+    w = workloads.Workload("t", T=T, H=256, E=8, K=2, routing="softmax", layout="contig",
+                           quant="fp8_ue8m0", align=128)
+    idx = np.array([[5, 1]] * T, dtype=np.int32).reshape(T, 2)
+    case = _custom_case(w, idx)
+    g = gh.run_gpu(w, case)
+    ref = gh.check_layout(w, case, g)
+    gh.check_dispatch(w, case, g, ref)
+    gh.check_combine(w, case, g, ref)
+
+
+def test_special_values_quantise_like_oracle():
+    """All-zero groups, groups under the 1e-4 clamp, outliers, exact ties, -0."""
+    T, H, E, K = 64, 512, 4, 2
+    rng = np.random.default_rng(5)
+    xf = rng.standard_normal((T, H)).astype(np.float32)
+    xf[0] = 0.0
+    xf[1] = -0.0
+    xf[2] *= 1e-7
+    xf[3, 5] = 3.0e38
+    xf[4] = np.round(xf[4] * 8) / 8
+    xf[5] *= 1e-30
+    xf[6, :128] = -1e-3
+    x = workloads.bf16_bits_from_f32(xf)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    wts = rng.random((T, K)).astype(np.float32)
+    for quant in ("fp8_f32", "fp8_ue8m0"):
+        w = workloads.Workload("sv", T=T, H=H, E=E, K=K, routing="softmax", layout="contig",
+                               quant=quant, align=16)
+        case = dict(idx=idx, w=wts, x=x, idx_d=torch.from_numpy(idx).cuda(),
+                    w_d=torch.from_numpy(wts).cuda(),
+                    x_d=torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
+        g = gh.run_gpu(w, case)
+        ref = gh.check_layout(w, case, g)
+        gh.check_dispatch(w, case, g, ref)
+
+
+@pytest.mark.parametrize("quant", ["none", "fp8_f32", "fp8_ue8m0"])
+def test_masked_repack_matches_masked_dispatch(quant):
+    from combine_expert_histogram_gb300 import binding as ep
+    w = workloads.CONFIGS["qwen3_30b_a3b_decode"].with_(quant=quant)
+    case = gh.make_case(w)
+    Lc = ep.ep_layout(case["idx_d"], w.E, kind="contig", align=128)
+    rows_c, sc_c, _ = ep.ep_dispatch(Lc, case["x_d"], quant)
+    slab, slab_sc, mm = ep.ep_masked_repack(Lc, rows_c, sc_c, quant, w.cap)
+    Lm = ep.ep_layout(case["idx_d"], w.E, kind="masked", capacity=w.cap)
+    rows_m, sc_m, _ = ep.ep_dispatch(Lm, case["x_d"], quant)
+    torch.cuda.synchronize()
+    cnt = Lc.expert_count.cpu().numpy()
+    assert np.array_equal(mm.cpu().numpy(), np.minimum(cnt, w.cap))
+    assert int(Lc.status.item()) == 0
+    ref = oracle.default().layout(case["idx"], w.E, "masked", cap=w.cap)
+    valid = np.nonzero(ref["row_src"] >= 0)[0]
+    v = torch.from_numpy(valid).cuda()
+    flat = slab.reshape(w.E * w.cap, -1)
+    assert torch.equal(flat.index_select(0, v).view(torch.uint8) if quant == "none" else flat.index_select(0, v),
+                       rows_m.index_select(0, v).view(torch.uint8) if quant == "none" else rows_m.index_select(0, v))
+    if quant != "none":
+        assert torch.equal(slab_sc.reshape(w.E * w.cap, -1).index_select(0, v).view(torch.int32),
+                           sc_m.index_select(0, v).view(torch.int32))
+
+
+def test_masked_repack_vs_oracle_with_overflow():
+    from combine_expert_histogram_gb300 import binding as ep
+    w = workloads.CONFIGS["qwen3_30b_a3b_decode"]
+    case = gh.make_case(w)
+    cap = 12  # most experts overflow
+    Lc = ep.ep_layout(case["idx_d"], w.E, kind="contig", align=128)
+    rows_c, sc_c, _ = ep.ep_dispatch(Lc, case["x_d"], "fp8_f32")
+    slab = torch.full((w.E, cap, w.H), gh.SENTINEL_U8, dtype=torch.uint8, device="cuda")
+    slab_sc = torch.zeros((w.E, cap, w.H // 128), dtype=torch.float32, device="cuda")
+    ep.ep_masked_repack(Lc, rows_c, sc_c, "fp8_f32", cap, slab=slab, slab_scales=slab_sc)
+    torch.cuda.synchronize()
+    orc = oracle.default()
+    rows_np = rows_c.cpu().numpy()
+    sc_np = sc_c.cpu().numpy()
+    o_slab, o_ss, o_mm, o_st = orc.masked_repack(rows_np, sc_np, w.H, "fp8_f32",
+                                                 Lc.expert_offset.cpu().numpy(),
+                                                 Lc.expert_count.cpu().numpy(), w.E, cap,
+                                                 fill=gh.SENTINEL_U8)
+    assert o_st == 2 and int(Lc.status.item()) == 2
+    assert np.array_equal(slab.reshape(w.E * cap, -1).cpu().numpy(), o_slab)
+    m = np.repeat(np.arange(cap)[None, :] < o_mm[:, None], 1).reshape(-1)
+    assert np.array_equal(slab_sc.reshape(w.E * cap, -1).cpu().numpy()[m], o_ss[m])
