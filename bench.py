@@ -148,6 +148,24 @@ class ClockSampler:
                 "samples": len(inwin), "window": window}
 
 
+# ------------------------------------------------------------ replicas
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank number over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tokens_per_s(tokens_per_rank: int, steps: int, world: int, max_elapsed_ms: float):
+    """Whole-job throughput: tokens of all replicas / the slowest rank's time."""
+    return tokens_per_rank * steps * world / (max_elapsed_ms * 1e-3)
+
+
 # ------------------------------------------------------------ CPU baseline
 def oracle_tokens_per_s(w, idx, wts, x, y_host, n_tokens):
     """Run the oracle's layout + dispatch + combine on the first n_tokens tokens."""
@@ -299,11 +317,7 @@ def run_ours(args, w):
     if sampler:
         time.sleep(0.15)
         sampler.stop()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), dev if world > 1 else None)
 
     seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
                     for e in evs])
@@ -324,8 +338,7 @@ def run_ours(args, w):
     if rank != 0:
         dist.destroy_process_group()
         return
-    tokens = w.T * args.steps * world
-    value = tokens / (elapsed_ms * 1e-3)
+    value = aggregate_tokens_per_s(w.T, args.steps, world, elapsed_ms)
     dom = max(("dispatch", "combine"), key=lambda k: kern[k]["us"])
     traffic = combine_traffic() if dom == "combine" else None
     achieved = kern[dom]["GB/s"]

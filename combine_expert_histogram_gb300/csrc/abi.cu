@@ -130,10 +130,10 @@ ep_status_t ep_dispatch(const ep_layout_t *L, const void *x, int32_t hidden, ep_
     if (st != EP_OK) return st;
     st = check_hidden(hidden, quant);
     if (st != EP_OK) return st;
+    if (L->num_tokens == 0) return EP_OK;  // nothing to move
     if ((topk_w == nullptr) != (row_w == nullptr)) return EP_ERR_INVALID_ARG;
     if (!aligned(topk_w, 4) || !aligned(row_w, 4)) return EP_ERR_INVALID_ARG;
     if (quant != EP_QUANT_NONE && (!out_scales || !aligned(out_scales, 4))) return EP_ERR_INVALID_ARG;
-    if (L->num_tokens == 0) return EP_OK;
     if (!x || !out_rows || !aligned(x, 16) || !aligned(out_rows, 16)) return EP_ERR_INVALID_ARG;
     return from_cuda(launch_dispatch(*L, x, hidden, quant, out_rows, out_scales, topk_w, row_w,
                                      reinterpret_cast<cudaStream_t>(stream)));

@@ -14,7 +14,7 @@ if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
 GUARD = 4096
-PAT = 0x5A5A5A5A - (1 << 32)  # int32 pattern
+PAT = 0x5A5A5A5A  # int32 guard pattern
 
 
 def _guarded(n, dtype=torch.int32):
