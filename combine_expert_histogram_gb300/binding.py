@@ -52,7 +52,8 @@ class _Layout(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("ep_status_str", "ep_rows_capacity", "ep_scale_cols", "ep_layout_workspace_bytes",
-           "ep_layout", "ep_dispatch", "ep_combine", "ep_masked_repack")
+           "ep_layout", "ep_dispatch", "ep_combine", "ep_masked_repack", "ep_layout_noalloc")
+NOALLOC_SCRATCH_BYTES = 256 * 1024
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -82,6 +83,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ep_combine.argtypes = [LP, P, I32, P, P, P]
     L.ep_masked_repack.restype = ctypes.c_int
     L.ep_masked_repack.argtypes = [LP, P, P, I32, ctypes.c_int, I32, P, P, P, P]
+    L.ep_layout_noalloc.restype = ctypes.c_int
+    L.ep_layout_noalloc.argtypes = [P, LP, P]
     if path == LIB_PATH:
         _lib = L
     return L
@@ -287,3 +290,21 @@ def ep_masked_repack(layout: Layout, rows: torch.Tensor, row_scales: Optional[to
                                            _ptr(slab_scales), _ptr(masked_m), _stream(stream))
     _check(code, "ep_masked_repack")
     return slab, slab_scales, masked_m
+
+
+def ep_layout_noalloc(topk_idx: torch.Tensor, out: Layout, stream=None) -> Layout:
+    """ep_layout with the library's fixed scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory; ``out`` must be a layout
+    whose arrays the caller already owns (``out.workspace`` is ignored).  Calls
+    share the library's one scratch array, so calls that overlap on the GPU race.
+    """
+    if topk_idx.dtype != torch.int32 or topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be int32 [T, K]")
+    T, K = topk_idx.shape
+    if (out.num_tokens, out.num_topk) != (T, K):
+        raise ValueError("layout shape does not match topk_idx")
+    code = load_library().ep_layout_noalloc(_ptr(topk_idx) if T * K else None,
+                                            ctypes.byref(out.struct()), _stream(stream))
+    _check(code, "ep_layout_noalloc")
+    return out

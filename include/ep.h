@@ -227,6 +227,27 @@ ep_status_t ep_masked_repack(const ep_layout_t *layout, const void *rows,
                              int32_t capacity, void *slab, void *slab_scales,
                              int32_t *masked_m, ep_stream_t stream);
 
+/*
+ * ep_layout_noalloc -- ep_layout with its scratch taken from a fixed array
+ * inside the library, for callers that cannot allocate device memory (a
+ * serving runtime that reserves all memory at start-up and forbids later
+ * allocation, a plugin handed only its input and output buffers, C code
+ * without a device allocator).  The pages have no counterpart to this call.
+ *
+ *   Same arguments and results as ep_layout, minus the workspace.
+ *   The array holds EP_NOALLOC_SCRATCH_BYTES on every GPU that loads the
+ *   library, until the process exits.  A shape whose ep_layout_workspace_bytes()
+ *   exceeds it is rejected with EP_ERR_CAPACITY before any launch.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make it before any stream capture.  All calls share the
+ *   array: calls whose work overlaps on the GPU race and must be ordered by
+ *   the caller (one stream, or events).  Nothing in the array needs clearing
+ *   between calls.
+ */
+#define EP_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+ep_status_t ep_layout_noalloc(const int32_t *topk_idx, const ep_layout_t *layout,
+                              ep_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
