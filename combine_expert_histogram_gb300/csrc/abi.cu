@@ -116,7 +116,9 @@ ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *L, void *works
     ep_status_t st = check_layout(L);
     if (st != EP_OK) return st;
     if (L->num_tokens > 0 && (!topk_idx || !aligned(topk_idx, 4))) return EP_ERR_INVALID_ARG;
-    const size_t need = layout_plan(*L).ws_bytes;
+    const LayoutPlan plan = layout_plan(*L);
+    if (plan.smem > 227 * 1024) return EP_ERR_UNSUPPORTED;  // more entries than one CTA can rank
+    const size_t need = plan.ws_bytes;
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 4)))
         return EP_ERR_INVALID_ARG;
     return from_cuda(launch_layout(topk_idx, *L, static_cast<int32_t *>(workspace),

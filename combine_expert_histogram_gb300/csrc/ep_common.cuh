@@ -41,18 +41,20 @@ __device__ __forceinline__ void st_v4(void *p, uint4 v) {
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-// Exclusive scan over n <= 2*NT values produced by value(i), by one CTA of NT
-// threads.  out[i] = value(0) + ... + value(i-1) for i in [0, n], out[n] = total.
-// `tmp` holds NT/32 ints of shared memory.  Must be reached by every thread.
+// Exclusive scan over n values produced by value(i), by one CTA of NT threads:
+// out[i] = value(0) + ... + value(i-1) for i in [0, n], out[n] = total.  Thread t
+// owns the contiguous run [t*ipt, (t+1)*ipt), ipt = ceil(n/NT).  `tmp` holds
+// NT/32 ints of shared memory.  Must be reached by every thread of the CTA.
 template <int NT, typename F>
 __device__ __forceinline__ void block_exclusive_scan(int n, F value, int32_t *out,
                                                      int32_t *tmp) {
     static_assert(NT % 32 == 0 && NT / 32 <= 32, "one warp scans the warp totals");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int i0 = 2 * threadIdx.x, i1 = i0 + 1;
-    const int v0 = i0 < n ? value(i0) : 0;
-    const int v1 = i1 < n ? value(i1) : 0;
-    const int s = v0 + v1;
+    const int ipt = (n + NT - 1) / NT;
+    const int b0 = min(n, (int)threadIdx.x * ipt);
+    const int b1 = min(n, b0 + ipt);
+    int s = 0;
+    for (int i = b0; i < b1; ++i) s += value(i);
     int incl = s;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -73,11 +75,12 @@ __device__ __forceinline__ void block_exclusive_scan(int n, F value, int32_t *ou
     }
     __syncthreads();
     const int excl = tmp[warp] + incl - s;
-    if (i0 < n) out[i0] = excl;
-    if (i1 < n) out[i1] = excl + v0;
-    if (i0 == n - 1) out[n] = excl + v0;
-    if (i1 == n - 1) out[n] = excl + s;
-    if (n == 0 && threadIdx.x == 0) out[0] = 0;
+    int run = excl;
+    for (int i = b0; i < b1; ++i) {
+        out[i] = run;
+        run += value(i);
+    }
+    if (threadIdx.x == NT - 1) out[n] = excl + s;  // runs past n are empty: this is the total
     __syncthreads();
 }
 

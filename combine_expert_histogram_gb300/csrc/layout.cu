@@ -6,74 +6,100 @@
 // (prefill) and masked (decode) layouts of SGLang PR "[Feature] Add DeepEPv2
 // (ElasticBuffer) MoE A2A backend", section "Supported scope".
 //
-// Design (deterministic, no global atomics on slot order):
-//   * the T*K entries are cut into tiles of <= 8192 entries, one CTA of 512
-//     threads each; every warp owns a contiguous chunk of its tile and keeps
-//     the chunk's ids in registers (one load per lane per 32 entries);
-//   * tile_hist_kernel (only when there are >= 2 tiles) writes each tile's
-//     expert histogram to the scratch workspace [tiles][E];
-//   * assign_kernel: every CTA rebuilds the totals and its tile's base per
-//     expert from the workspace (tiles x E ints from L2), scans the padded
-//     counts, then ranks its entries: per-warp histograms give each warp's
-//     starting slot per expert, and inside a warp __match_any_sync groups the
-//     lanes holding the same expert, so a lane's slot is its warp base plus
-//     the number of lower lanes in its group.  That order is exactly
-//     ascending (token, k);
-//   * extra CTAs (masked layouts) only write -1 into row_src for empty slots.
+// Design (deterministic, no global atomics on slot order; latency-bound, so
+// the goal is short dependency chains and every SM busy):
+//   * the T*K entries are cut into tiles of 2048 entries (more for huge
+//     inputs), one CTA of 256 threads per tile; warp w owns a contiguous
+//     chunk of its tile and lane l holds entries chunk + 32r + l, r < rounds,
+//     in registers (all loads issued up front);
+//   * lanes holding the same expert in a round find each other with
+//     ceil(log2(E+1)) independent __ballot_sync's (one per bit of the id);
+//     the mask is kept per round and reused for ranking;
+//   * tile_hist_kernel (only with >= 2 tiles) writes each tile's expert
+//     histogram to the scratch workspace [tiles][E];
+//   * assign_kernel: every CTA sums the workspace columns (independent L2
+//     loads) into the expert totals and its tile's base, scans the padded
+//     counts, turns per-warp histograms into per-warp starting slots, and
+//     gives each entry slot = warp base + #lower lanes with the same expert.
+//     That order is exactly ascending (token, k);
+//   * extra CTAs (masked layouts with row_src) only write -1 into row_src for
+//     empty slots.
 #include "ep_common.cuh"
 
 namespace ep {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRounds = 16;                   // 32-entry rounds per warp chunk
-constexpr int kMaxTile = kThreads * kRounds;  // 8192 entries
+constexpr int kRounds = 8;                    // 32-entry rounds per warp chunk
+constexpr int kTile = kThreads * kRounds;     // 2048 entries
+constexpr int kMaxBits = 11;                  // ids 0..1024 (1024 = "no expert")
 constexpr int kFillCtas = 128;
+constexpr int kSumChunk = 16;                 // workspace loads in flight per thread
 
 __host__ __device__ inline int round_up_pow2(int v, int a) { return (v + a - 1) & ~(a - 1); }
 
-// Load a warp chunk's ids: lane l gets entries c0 + 32*r + l, r < rounds.
-// Invalid ids (outside [0, E)) and entries past c1 read as -1; `bad` flags
-// rounds whose entry exists but holds an id outside [-1, E).
+// A warp chunk, kRounds entries per lane: ids (invalid ones mapped to E),
+// peer masks (lanes with the same id this round) and the bad-id flags.
+struct Chunk {
+    int ev[kRounds];
+    unsigned peers[kRounds];
+    unsigned bad;
+};
+
 __device__ __forceinline__ void load_chunk(const int32_t *__restrict__ idx, int c0, int c1,
-                                           int E, int (&ev)[kRounds], unsigned &bad) {
+                                           int E, int nbits, Chunk &c) {
     const int lane = threadIdx.x & 31;
-    bad = 0;
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
         const int i = c0 + r * 32 + lane;
-        ev[r] = i < c1 ? __ldg(idx + i) : -1;
+        c.ev[r] = i < c1 ? __ldg(idx + i) : -1;
+    }
+    c.bad = 0;
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        const int e = c.ev[r];
+        if (e < -1 || e >= E) c.bad |= 1u << r;
+        c.ev[r] = (e >= 0 && e < E) ? e : E;  // E = no expert
     }
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
-        if (ev[r] < -1 || ev[r] >= E) {
-            bad |= 1u << r;
-            ev[r] = -1;
+        const int v = c.ev[r];
+        unsigned m = kFullMask;
+#pragma unroll
+        for (int b = 0; b < kMaxBits; ++b) {
+            if (b < nbits) {  // warp-uniform
+                const unsigned bit = (v >> b) & 1u;
+                const unsigned bal = __ballot_sync(kFullMask, bit);
+                m &= bit ? bal : ~bal;
+            }
         }
+        c.peers[r] = m;
     }
 }
+
+__device__ __forceinline__ int id_bits(int E) { return 32 - __clz(E); }  // E itself must fit
 
 __global__ void __launch_bounds__(kThreads)
     tile_hist_kernel(const int32_t *__restrict__ idx, int TK, int E, int tile,
                      int32_t *__restrict__ ws, int32_t *__restrict__ status) {
     extern __shared__ int32_t hist[];  // [E]
     for (int e = threadIdx.x; e < E; e += kThreads) hist[e] = 0;
-    __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int start = blockIdx.x * tile;
     const int end = min(TK, start + tile);
-    const int chunk = tile / kWarps;
-    const int c0 = start + warp * chunk;
-    const int c1 = min(end, c0 + chunk);
-    int ev[kRounds];
-    unsigned bad;
-    load_chunk(idx, c0, c1, E, ev, bad);
+    Chunk c;
+    __syncthreads();  // hist zeroed
+    // tiles larger than kTile (huge inputs) are walked in kTile-sized passes
+    for (int base = start; base < end; base += kTile) {  // block-uniform
+        const int c0 = base + warp * kRounds * 32;
+        const int c1 = min(end, c0 + kRounds * 32);
+        load_chunk(idx, c0, c1, E, id_bits(E), c);
 #pragma unroll
-    for (int r = 0; r < kRounds; ++r) {
-        if (c0 + r * 32 >= c1) break;  // warp-uniform
-        const unsigned peers = __match_any_sync(kFullMask, ev[r]);
-        if (ev[r] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[ev[r]], __popc(peers));
+        for (int r = 0; r < kRounds; ++r) {
+            const int e = c.ev[r];
+            if (e < E && lane == __ffs(c.peers[r]) - 1) atomicAdd(&hist[e], __popc(c.peers[r]));
+        }
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kThreads) ws[(size_t)blockIdx.x * E + e] = hist[e];
@@ -92,9 +118,10 @@ struct AssignArgs {
 __global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
     extern __shared__ int32_t sm[];
     const int E = a.E;
-    int32_t *wh = sm;                  // [kWarps][E]: per-warp counts, then slot bases
-    int32_t *tot = wh + kWarps * E;    // [E] expert histogram
-    int32_t *off = tot + E;            // [E+1] first row of each expert
+    int32_t *wh = sm;                  // [passes][kWarps][E]: per-warp counts, then slot bases
+    const int passes = a.tile / kTile;
+    int32_t *tot = wh + passes * kWarps * E;  // [E] expert histogram
+    int32_t *off = tot + E;                   // [E+1] first row of each expert
     __shared__ int32_t scan_tmp[kWarps];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -102,52 +129,59 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
     const int tile_id = assigns ? blockIdx.x : 0;
     const int start = tile_id * a.tile;
     const int end = min(a.TK, start + a.tile);
-    const int chunk = a.tile / kWarps;
-    const int c0 = start + warp * chunk;
-    const int c1 = min(end, c0 + chunk);
     const bool need_hist = assigns || a.tiles == 1;
+    const int nbits = id_bits(E);
 
     // With one tile this is the only layout kernel: reset the status word
-    // before any error of this CTA is raised (ordered by the barrier below).
+    // before any error of this CTA is raised (ordered by the barriers below).
     if (a.tiles == 1 && blockIdx.x == 0 && threadIdx.x == 0) *a.status = EP_OK;
-    for (int j = threadIdx.x; j < kWarps * E; j += kThreads) wh[j] = 0;
-
-    int ev[kRounds];
-    unsigned bad = 0;
-    if (need_hist) load_chunk(a.idx, c0, c1, E, ev, bad);
+    for (int j = threadIdx.x; j < passes * kWarps * E; j += kThreads) wh[j] = 0;
     __syncthreads();
 
-    // 1. per-warp expert histogram of this tile
+    // 1. per-(pass, warp) expert histogram of this tile; chunks stay in registers
+    //    only for single-pass tiles (the common case), else they are reloaded.
+    Chunk c;
     if (need_hist) {
+        for (int p = 0; p < passes; ++p) {
+            const int c0 = start + p * kTile + warp * kRounds * 32;
+            const int c1 = min(end, c0 + kRounds * 32);
+            load_chunk(a.idx, c0, c1, E, nbits, c);
+            int32_t *row = wh + (p * kWarps + warp) * E;
 #pragma unroll
-        for (int r = 0; r < kRounds; ++r) {
-            if (c0 + r * 32 >= c1) break;
-            const unsigned peers = __match_any_sync(kFullMask, ev[r]);
-            if (ev[r] >= 0 && lane == __ffs(peers) - 1) wh[warp * E + ev[r]] += __popc(peers);
-            __syncwarp();
+            for (int r = 0; r < kRounds; ++r) {
+                const int e = c.ev[r];
+                if (e < E && lane == __ffs(c.peers[r]) - 1) row[e] += __popc(c.peers[r]);
+                __syncwarp();
+            }
         }
     }
     __syncthreads();
 
-    // 2. expert totals; per-warp counts -> per-warp starting slots
+    // 2. expert totals and this tile's base; per-warp counts -> starting slots
     for (int e = threadIdx.x; e < E; e += kThreads) {
         int total = 0, base = 0;
         if (a.tiles == 1) {
-            for (int w = 0; w < kWarps; ++w) total += wh[w * E + e];
+            for (int j = 0; j < passes * kWarps; ++j) total += wh[j * E + e];
         } else {
-            for (int b = 0; b < a.tiles; ++b) {
-                const int c = __ldcg(a.ws + (size_t)b * E + e);
-                base += b < tile_id ? c : 0;
-                total += c;
+            for (int b0 = 0; b0 < a.tiles; b0 += kSumChunk) {
+                int v[kSumChunk];
+#pragma unroll
+                for (int u = 0; u < kSumChunk; ++u)
+                    v[u] = b0 + u < a.tiles ? __ldcg(a.ws + (size_t)(b0 + u) * E + e) : 0;
+#pragma unroll
+                for (int u = 0; u < kSumChunk; ++u) {
+                    base += b0 + u < tile_id ? v[u] : 0;
+                    total += v[u];
+                }
             }
         }
         tot[e] = total;
         if (assigns) {
             int run = base;
-            for (int w = 0; w < kWarps; ++w) {
-                const int c = wh[w * E + e];
-                wh[w * E + e] = run;
-                run += c;
+            for (int j = 0; j < passes * kWarps; ++j) {  // (pass, warp) order = entry order
+                const int cnt = wh[j * E + e];
+                wh[j * E + e] = run;
+                run += cnt;
             }
         }
     }
@@ -176,29 +210,35 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
 
     // 4. stable slots: warp base + rank among lower lanes with the same expert
     if (assigns) {
+        for (int p = 0; p < passes; ++p) {
+            const int c0 = start + p * kTile + warp * kRounds * 32;
+            const int c1 = min(end, c0 + kRounds * 32);
+            if (passes > 1) load_chunk(a.idx, c0, c1, E, nbits, c);
+            int32_t *row = wh + (p * kWarps + warp) * E;
 #pragma unroll
-        for (int r = 0; r < kRounds; ++r) {
-            const int i0 = c0 + r * 32;
-            if (i0 >= c1) break;
-            const int e = ev[r];
-            const unsigned peers = __match_any_sync(kFullMask, e);
-            const int slot = e >= 0 ? wh[warp * E + e] + __popc(peers & lanemask_lt()) : 0;
-            __syncwarp();
-            if (e >= 0 && lane == __ffs(peers) - 1) wh[warp * E + e] += __popc(peers);
-            __syncwarp();
-            const int i = i0 + lane;
-            if (i < c1) {
-                int dst = -1;
-                if (bad & (1u << r)) {
-                    raise_status(a.status, EP_ERR_BAD_EXPERT_ID);
-                } else if (e >= 0) {
-                    if (masked && slot >= cap)
-                        raise_status(a.status, EP_ERR_CAPACITY);
-                    else
-                        dst = off[e] + slot;
+            for (int r = 0; r < kRounds; ++r) {
+                const int i0 = c0 + r * 32;
+                if (i0 >= c1) break;  // warp-uniform
+                const int e = c.ev[r];
+                const unsigned peers = c.peers[r];
+                const int slot = e < E ? row[e] + __popc(peers & lanemask_lt()) : 0;
+                __syncwarp();
+                if (e < E && lane == __ffs(peers) - 1) row[e] += __popc(peers);
+                __syncwarp();
+                const int i = i0 + lane;
+                if (i < c1) {
+                    int dst = -1;
+                    if (c.bad & (1u << r)) {
+                        raise_status(a.status, EP_ERR_BAD_EXPERT_ID);
+                    } else if (e < E) {
+                        if (masked && slot >= cap)
+                            raise_status(a.status, EP_ERR_CAPACITY);
+                        else
+                            dst = off[e] + slot;
+                    }
+                    a.dst_row[i] = dst;
+                    if (dst >= 0 && a.row_src) a.row_src[dst] = i;
                 }
-                a.dst_row[i] = dst;
-                if (dst >= 0 && a.row_src) a.row_src[dst] = i;
             }
         }
     }
@@ -218,21 +258,22 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
 LayoutPlan layout_plan(const ep_layout_t &L) {
     LayoutPlan p{};
     const long long TK = (long long)L.num_tokens * L.num_topk;
-    if (TK <= kMaxTile) {
-        p.tiles = 1;
-        p.tile = (int)((TK + 511) / 512 * 512);
-        if (p.tile == 0) p.tile = 512;
-    } else {
-        p.tiles = (int)((TK + kMaxTile - 1) / kMaxTile);
-        long long per = (TK + p.tiles - 1) / p.tiles;
-        p.tile = (int)((per + 511) / 512 * 512);
-        p.tiles = (int)((TK + p.tile - 1) / p.tile);
+    // tiles of kTile entries; inputs beyond 128 tiles grow the tile by whole
+    // kTile passes instead, which bounds the workspace and the column sums
+    long long tiles = (TK + kTile - 1) / kTile;
+    if (tiles < 1) tiles = 1;
+    int passes = 1;
+    if (tiles > 128) {
+        passes = (int)((tiles + 127) / 128);
+        tiles = (TK + (long long)kTile * passes - 1) / ((long long)kTile * passes);
     }
+    p.tiles = (int)tiles;
+    p.tile = kTile * passes;
     const bool fill = L.kind == EP_LAYOUT_MASKED && L.row_src != nullptr;
     p.grid = p.tiles;
-    if (fill) p.grid = p.tiles > kFillCtas ? p.tiles : (L.num_experts < kFillCtas ? L.num_experts : kFillCtas);
+    if (fill && p.grid < kFillCtas) p.grid = L.num_experts < kFillCtas ? L.num_experts : kFillCtas;
     if (p.grid < p.tiles) p.grid = p.tiles;
-    p.smem = sizeof(int32_t) * ((size_t)kWarps * L.num_experts + 2 * (size_t)L.num_experts + 1);
+    p.smem = sizeof(int32_t) * ((size_t)passes * kWarps * L.num_experts + 2 * (size_t)L.num_experts + 1);
     p.ws_bytes = p.tiles > 1 ? sizeof(int32_t) * (size_t)p.tiles * L.num_experts : 0;
     return p;
 }

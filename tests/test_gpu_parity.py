@@ -54,6 +54,11 @@ MID = [
                        layout="masked", quant="fp8_ue8m0", cap=16, R=16, seed=8),
     workloads.Workload("h128", T=5000, H=128, E=32, K=2, routing="softmax",
                        layout="contig", quant="fp8_f32", align=32, seed=9),
+    # > 128 tiles of 2048 entries: tiles of several passes
+    workloads.Workload("multipass", T=40000, H=128, E=64, K=8, routing="softmax",
+                       layout="contig", quant="fp8_ue8m0", align=128, R=4, seed=10),
+    workloads.Workload("multipass_e1024", T=40000, H=128, E=1024, K=8, routing="zipf",
+                       layout="masked", quant="fp8_f32", cap=2048, R=8, seed=11),
 ]
 
 
