@@ -299,7 +299,12 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     L.check_status()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # Per-kernel events go on every --event-every'th step only: an event
+    # between two kernels also cuts the programmatic (overlapped) launch of
+    # the next one, so the other steps run exactly as a caller would run them.
+    every = max(1, args.event_every)
+    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+           for i in range(0, args.steps, every)}
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -308,7 +313,7 @@ def run_ours(args, w):
     t_wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step(evs.get(i))
     end.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -320,7 +325,7 @@ def run_ours(args, w):
     elapsed_ms = max_over_ranks(start.elapsed_time(end), dev if world > 1 else None)
 
     seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
-                    for e in evs])
+                    for e in evs.values()])
     lay_ms, disp_ms, comb_ms = seg.mean(axis=0)
     ab = algorithmic_bytes(w)
     peak, peak_src = peak_hbm()
@@ -358,6 +363,7 @@ def run_ours(args, w):
                           f"(L2 129 MB); no flush")},
         "step_gbs": round(sum(ab.values()) * args.steps * world / (elapsed_ms * 1e-3) / 1e9, 1),
         "kernels": kern,
+        "kernel_events": f"per-kernel events on {len(evs)} of {args.steps} timed steps",
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
@@ -369,11 +375,109 @@ def run_ours(args, w):
         line["clocks"] = sampler.summary(t_wall0, t_wall1)
     if e2e:
         line["e2e"] = e2e
+    if not args.skip_decode:
+        line["decode"] = measure_decode(ep, dev)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, idx, wts, x)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_decode(ep, dev, reps=50):
+    """Decode shapes (masked layouts): per-step latency with L2 flushed before every
+    rep, CUDA-graph replay latency (warm L2), and the masked repack on its own."""
+    import torch
+    flush = torch.empty(2 * L2_BYTES // 4 * 4, dtype=torch.uint8, device=dev)  # 2x L2
+    res = {}
+    for name in ("qwen3_30b_a3b_decode", "dsv3_decode"):
+        w = workloads.CONFIGS[name]
+        idx, wts, x = workloads.make_inputs(w)
+        idx_d = torch.from_numpy(idx).to(dev)
+        w_d = torch.from_numpy(wts).to(dev)
+        x_d = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        L = ep.new_layout(w.T, w.K, w.E, "masked", capacity=w.cap, device=dev)
+        rows = L.rows_capacity
+        out_rows = torch.empty((rows, w.H), dtype=torch.uint8, device=dev)
+        sc = torch.empty((rows, ep.ep_scale_cols(w.H, w.quant)), device=dev,
+                         dtype=torch.float32 if w.quant == "fp8_f32" else torch.int32)
+        y = workloads.make_expert_outputs(rows, w.H, seed=3, device=dev)
+        out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+        s = torch.cuda.Stream(device=dev)
+
+        def step():
+            ep.ep_layout(idx_d, w.E, out=L, stream=s)
+            ep.ep_dispatch(L, x_d, w.quant, out_rows=out_rows, out_scales=sc, stream=s)
+            ep.ep_combine(L, y, w_d, out=out, stream=s)
+
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                step()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+        with torch.cuda.stream(s):
+            for i in range(reps):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(s)
+                ep.ep_layout(idx_d, w.E, out=L, stream=s)
+                ev[i][1].record(s)
+                ep.ep_dispatch(L, x_d, w.quant, out_rows=out_rows, out_scales=sc, stream=s)
+                ev[i][2].record(s)
+                ep.ep_combine(L, y, w_d, out=out, stream=s)
+                ev[i][3].record(s)
+        torch.cuda.synchronize()
+        seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+                        for e in ev]) * 1e3
+        med = np.median(seg, axis=0)
+        ab = algorithmic_bytes(w)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        graph_us = a.elapsed_time(b) * 1e3 / reps
+        # masked repack from a contiguous layout (same routing), L2 flushed
+        Lc = ep.new_layout(w.T, w.K, w.E, "contig", align=128, device=dev)
+        ep.ep_layout(idx_d, w.E, out=Lc)
+        rc = Lc.rows_capacity
+        rows_c = torch.empty((rc, w.H), dtype=torch.uint8, device=dev)
+        sc_c = torch.empty((rc, sc.shape[1]), dtype=sc.dtype, device=dev)
+        ep.ep_dispatch(Lc, x_d, w.quant, out_rows=rows_c, out_scales=sc_c)
+        slab = torch.empty_like(out_rows)
+        slab_sc = torch.empty_like(sc)
+        mm = torch.empty(w.E, dtype=torch.int32, device=dev)
+        rts = []
+        for i in range(reps):
+            flush.fill_(i & 0xFF)
+            a.record()
+            ep.ep_masked_repack(Lc, rows_c, sc_c, w.quant, w.cap, slab=slab, slab_scales=slab_sc,
+                                masked_m=mm)
+            b.record()
+            torch.cuda.synchronize()
+            rts.append(a.elapsed_time(b) * 1e3)
+        rep_us = float(np.median(rts))
+        rep_bytes = 2 * w.T * w.K * (w.H + 4 * sc.shape[1])  # valid rows read + written
+        res[name] = {
+            "T": w.T, "H": w.H, "E": w.E, "K": w.K, "cap": w.cap, "quant": w.quant,
+            "l2_flushed_us": {"layout": round(med[0], 2), "dispatch": round(med[1], 2),
+                              "combine": round(med[2], 2), "step": round(float(med.sum()), 2)},
+            "dispatch_GBps": round(ab["dispatch"] / (med[1] * 1e-6) / 1e9, 1),
+            "combine_GBps": round(ab["combine"] / (med[2] * 1e-6) / 1e9, 1),
+            "tokens_per_s_flushed": round(w.T / (med.sum() * 1e-6), 1),
+            "graph_replay_us_warm_l2": round(graph_us, 2),
+            "masked_repack_us": round(rep_us, 2),
+            "masked_repack_GBps": round(rep_bytes / (rep_us * 1e-6) / 1e9, 1),
+        }
+        del y, out_rows, slab, rows_c
+        torch.cuda.empty_cache()
+    return res
 
 
 def measure_e2e(ep, w, L, idx, wts, x, y_dev, out_rows, out_scales, dev, stream, args):
@@ -435,6 +539,10 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer e2e leg")
+    ap.add_argument("--event-every", type=int, default=10,
+                    help="per-kernel CUDA events on every N-th timed step")
+    ap.add_argument("--skip-decode", action="store_true",
+                    help="omit the decode-shape (masked layout) measurements")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (small cases for profiling; not a bench line)")
     args = ap.parse_args()

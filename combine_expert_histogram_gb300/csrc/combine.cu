@@ -25,6 +25,9 @@ __global__ void __launch_bounds__(kThreads)
     combine_kernel(const uint16_t *__restrict__ y, int K, int H, long long n_chunks,
                    const int32_t *__restrict__ dst_row, const float *__restrict__ topk_w,
                    uint16_t *__restrict__ out) {
+    // Launched as a programmatic dependent: wait for the previous kernel on
+    // the stream (it may have produced y) before reading anything.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long c = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (c >= n_chunks) return;
     const int CH = H >> 3;
@@ -78,10 +81,9 @@ cudaError_t launch_combine(const ep_layout_t &L, const void *y, int H, const flo
     if (T == 0) return cudaSuccess;
     const long long n = (long long)T * (H / 8);
     const long long blocks = (n + kThreads - 1) / kThreads;
-    combine_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(
-        static_cast<const uint16_t *>(y), K, H, n, L.dst_row, topk_w,
-        static_cast<uint16_t *>(out));
-    return cudaGetLastError();
+    return launch_kernel(combine_kernel, (int)blocks, kThreads, 0, stream, true,
+                         static_cast<const uint16_t *>(y), K, H, n, L.dst_row, topk_w,
+                         static_cast<uint16_t *>(out));
 }
 
 }  // namespace ep

@@ -6,14 +6,23 @@
 // "Implementation": Hopper FP32 scales and Blackwell packed UE8M0 scales) and
 // the vLLM tools/ep_kernels deepep_v2 commit ("FP8 block-quantized dispatch").
 //
-// HBM-bound: each token row is read once and written K times.  Work mapping:
-//   FP8:  8 lanes own one 128-element group (16 bf16 = 32 B per lane, two
-//         16-byte loads); a warp covers 4 consecutive groups; the group amax
-//         is reduced with three xor-shuffles inside the 8 lanes; each lane
-//         converts its 16 values to 16 E4M3 bytes and stores them as one
-//         16-byte vector to each of the K destination rows, so every warp
-//         store is 512 contiguous bytes.
-//   bf16: one lane per 16-byte chunk; K 16-byte stores.
+// HBM-bound: each token row is read once and written K times (80 % of the
+// bytes are writes).  One CTA owns one token:
+//   1. its threads load the row (16 bf16 = two 16-byte loads per thread),
+//      8 consecutive lanes per 128-element group; the group amax is reduced
+//      with three xor-shuffles inside those 8 lanes;
+//   2. each thread converts its 16 values to E4M3 and writes them, with the
+//      group's scale, into a shared-memory copy of the output row;
+//   3. after a proxy fence, a wait for the layout kernels (dispatch is
+//      launched as their programmatic dependent, so steps 1-2 overlap them)
+//      and a barrier, one thread issues one
+//      cp.async.bulk store per destination row (the whole H-byte row, and the
+//      fp32 scale row when its size is a multiple of 16 bytes), so the TMA
+//      engine writes K contiguous rows while the SM moves on;
+//   4. the thread waits for the bulk stores to finish reading shared memory
+//      before the CTA exits.
+// Scale rows that are not a multiple of 16 bytes (packed UE8M0, or fp32 with
+// H/128 not a multiple of 4) are written by plain 4-byte stores.
 #include <cuda_fp8.h>
 
 #include "ep_common.cuh"
@@ -21,7 +30,7 @@
 namespace ep {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kMaxThreads = 512;
 
 __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d) {
     // __nv_cvt_float2_to_fp8x2: round to nearest even, saturate to +-448;
@@ -31,109 +40,155 @@ __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d) {
     return (lo & 0xffffu) | (hi << 16);
 }
 
-template <int Q>
-__global__ void __launch_bounds__(kThreads)
-    dispatch_fp8_kernel(const uint16_t *__restrict__ x, int K, int H, long long n_groups,
-                        const int32_t *__restrict__ dst_row, uint8_t *__restrict__ out,
-                        void *__restrict__ scales, const float *__restrict__ topk_w,
-                        float *__restrict__ row_w) {
-    const int lane = threadIdx.x & 31;
-    const int sub = lane & 7;
-    const long long grp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 3;
-    if (grp >= n_groups) return;  // whole 8-lane groups leave together
-    const unsigned gmask = 0xffu << (lane & 24);
-    const int G = H >> 7;
-    const int t = (int)(grp / G);
-    const int g = (int)(grp - (long long)t * G);
-
-    const uint16_t *src = x + (size_t)t * H + g * 128 + sub * 16;
-    const uint4 a = ld_stream(src);
-    const uint4 b = ld_stream(src + 8);
-    float v[16];
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        v[2 * i] = bf16_lo(w[i]);
-        v[2 * i + 1] = bf16_hi(w[i]);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 4));
-    amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
-
-    // s = max(amax, 1e-4) / 448, an IEEE round-to-nearest division.
-    const float s = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
-    uint4 q;
-    uint32_t ebyte = 0;
-    if (Q == EP_QUANT_FP8_F32) {
-        q.x = fp8x4(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s), __fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
-        q.y = fp8x4(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s), __fdiv_rn(v[6], s), __fdiv_rn(v[7], s));
-        q.z = fp8x4(__fdiv_rn(v[8], s), __fdiv_rn(v[9], s), __fdiv_rn(v[10], s), __fdiv_rn(v[11], s));
-        q.w = fp8x4(__fdiv_rn(v[12], s), __fdiv_rn(v[13], s), __fdiv_rn(v[14], s), __fdiv_rn(v[15], s));
-    } else {
-        // scale rounded up to a power of two 2^(e-127); multiply by 2^(127-e)
-        const uint32_t bits = __float_as_uint(s);
-        const int e = (int)((bits >> 23) & 0xffu) + ((bits & 0x7fffffu) != 0u);
-        const float inv = __uint_as_float((uint32_t)(254 - e) << 23);
-        q.x = fp8x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv), __fmul_rn(v[3], inv));
-        q.y = fp8x4(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv), __fmul_rn(v[6], inv), __fmul_rn(v[7], inv));
-        q.z = fp8x4(__fmul_rn(v[8], inv), __fmul_rn(v[9], inv), __fmul_rn(v[10], inv), __fmul_rn(v[11], inv));
-        q.w = fp8x4(__fmul_rn(v[12], inv), __fmul_rn(v[13], inv), __fmul_rn(v[14], inv), __fmul_rn(v[15], inv));
-        ebyte = (uint32_t)e;
-    }
-
-    // UE8M0 with H a multiple of 512: the warp's 4 groups are bytes 0..3 of
-    // one int32 scale word of one token; lane 0 packs and stores it.
-    const bool packed_word = Q == EP_QUANT_FP8_UE8M0 && (G & 3) == 0;
-    uint32_t word = 0;
-    if (packed_word) {
-        const uint32_t e1 = __shfl_sync(kFullMask, ebyte, 8);
-        const uint32_t e2 = __shfl_sync(kFullMask, ebyte, 16);
-        const uint32_t e3 = __shfl_sync(kFullMask, ebyte, 24);
-        word = ebyte | (e1 << 8) | (e2 << 16) | (e3 << 24);
-    }
-    const int P4 = ((G + 3) >> 2) * 4;  // scale bytes per row, UE8M0
-
-    const int32_t *drow = dst_row + (size_t)t * K;
-    for (int k = 0; k < K; ++k) {
-        const int d = __ldg(drow + k);
-        if (d < 0) continue;
-        st_v4(out + (size_t)d * H + g * 128 + sub * 16, q);
-        if (sub == 0) {
-            if (Q == EP_QUANT_FP8_F32) {
-                reinterpret_cast<float *>(scales)[(size_t)d * G + g] = s;
-            } else if (packed_word) {
-                if (lane == 0) reinterpret_cast<uint32_t *>(scales)[(size_t)d * (P4 >> 2) + (g >> 2)] = word;
-            } else {
-                uint8_t *srow = reinterpret_cast<uint8_t *>(scales) + (size_t)d * P4;
-                srow[g] = (uint8_t)ebyte;
-                if (g == G - 1)
-                    for (int p = G; p < P4; ++p) srow[p] = 127;  // 2^0 in unused bytes
-            }
-            if (row_w && g == 0) row_w[d] = __ldg(topk_w + (size_t)t * K + k);
-        }
-    }
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__global__ void __launch_bounds__(kThreads)
-    dispatch_bf16_kernel(const uint16_t *__restrict__ x, int K, int H, long long n_chunks,
-                         const int32_t *__restrict__ dst_row, uint16_t *__restrict__ out,
-                         const float *__restrict__ topk_w, float *__restrict__ row_w) {
-    const long long c = (long long)blockIdx.x * kThreads + threadIdx.x;
-    if (c >= n_chunks) return;
-    const int CH = H >> 3;
-    const int t = (int)(c / CH);
-    const int j = (int)(c - (long long)t * CH);
-    const uint4 v = ld_stream(x + (size_t)t * H + j * 8);
-    const int32_t *drow = dst_row + (size_t)t * K;
-    for (int k = 0; k < K; ++k) {
-        const int d = __ldg(drow + k);
-        if (d < 0) continue;
-        st_v4(out + (size_t)d * H + j * 8, v);
-        if (row_w && j == 0) row_w[d] = __ldg(topk_w + (size_t)t * K + k);
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// shared memory to global memory, tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_addr(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the TMA (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int Q>
+__global__ void __launch_bounds__(kMaxThreads)
+    dispatch_kernel(const uint16_t *__restrict__ x, int K, int H,
+                    const int32_t *__restrict__ dst_row, uint8_t *__restrict__ out,
+                    void *__restrict__ scales, const float *__restrict__ topk_w,
+                    float *__restrict__ row_w, bool bulk_scales) {
+    // bulk_scales: fp32 scale rows are a multiple of 16 bytes and `scales` is
+    // 16-byte aligned, so they go out with the TMA too
+    extern __shared__ __align__(128) uint8_t stage[];
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int G = H >> 7;
+    // staged bytes: the row (H fp8 or 2H bf16), then the scale row
+    const int row_bytes = Q == EP_QUANT_NONE ? 2 * H : H;
+    const int P4 = ((G + 3) >> 2) * 4;  // UE8M0 scale bytes per row
+    const int scale_bytes = Q == EP_QUANT_FP8_F32 ? 4 * G : Q == EP_QUANT_FP8_UE8M0 ? P4 : 0;
+    uint8_t *srow = stage;
+    uint8_t *sscale = stage + row_bytes;
+    __shared__ int32_t sdst[EP_MAX_TOPK];
+
+    if (Q == EP_QUANT_FP8_UE8M0 && threadIdx.x < P4 - G) sscale[G + threadIdx.x] = 127;  // 2^0
+
+    const uint16_t *xr = x + (size_t)t * H;
+    if (Q == EP_QUANT_NONE) {
+        for (int j = threadIdx.x; j < H / 8; j += blockDim.x)
+            reinterpret_cast<uint4 *>(srow)[j] = ld_stream(xr + j * 8);
+    } else {
+        // slot j: group j/8, elements (j%8)*16 .. +15 of that group
+        for (int j = threadIdx.x; j < G * 8; j += blockDim.x) {  // block-uniform trip count per warp
+            const int g = j >> 3, sub = j & 7;
+            const unsigned gmask = 0xffu << (lane & 24);
+            const uint4 a = ld_stream(xr + g * 128 + sub * 16);
+            const uint4 b = ld_stream(xr + g * 128 + sub * 16 + 8);
+            float v[16];
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[2 * i] = bf16_lo(w[i]);
+                v[2 * i + 1] = bf16_hi(w[i]);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 4));
+            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+            // s = max(amax, 1e-4) / 448, an IEEE round-to-nearest division.
+            const float s = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+            uint4 q;
+            if (Q == EP_QUANT_FP8_F32) {
+                q.x = fp8x4(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s), __fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
+                q.y = fp8x4(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s), __fdiv_rn(v[6], s), __fdiv_rn(v[7], s));
+                q.z = fp8x4(__fdiv_rn(v[8], s), __fdiv_rn(v[9], s), __fdiv_rn(v[10], s), __fdiv_rn(v[11], s));
+                q.w = fp8x4(__fdiv_rn(v[12], s), __fdiv_rn(v[13], s), __fdiv_rn(v[14], s), __fdiv_rn(v[15], s));
+                if (sub == 0) reinterpret_cast<float *>(sscale)[g] = s;
+            } else {
+                // scale rounded up to a power of two 2^(e-127); multiply by 2^(127-e)
+                const uint32_t bits = __float_as_uint(s);
+                const int e = (int)((bits >> 23) & 0xffu) + ((bits & 0x7fffffu) != 0u);
+                const float inv = __uint_as_float((uint32_t)(254 - e) << 23);
+                q.x = fp8x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv), __fmul_rn(v[3], inv));
+                q.y = fp8x4(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv), __fmul_rn(v[6], inv), __fmul_rn(v[7], inv));
+                q.z = fp8x4(__fmul_rn(v[8], inv), __fmul_rn(v[9], inv), __fmul_rn(v[10], inv), __fmul_rn(v[11], inv));
+                q.w = fp8x4(__fmul_rn(v[12], inv), __fmul_rn(v[13], inv), __fmul_rn(v[14], inv), __fmul_rn(v[15], inv));
+                if (sub == 0) sscale[g] = (uint8_t)e;
+            }
+            reinterpret_cast<uint4 *>(srow)[j] = q;
+        }
     }
+    fence_proxy_async_smem();
+    // x was complete before the layout started; dst_row is the layout's
+    // output: wait for it (a no-op without a programmatic edge).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x < K) sdst[threadIdx.x] = dst_row[(size_t)t * K + threadIdx.x];
+    __syncthreads();
+
+    // one thread hands the staged row to the TMA engine, once per destination
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < K; ++k) {
+            const int d = sdst[k];
+            if (d < 0) continue;
+            bulk_store(out + (size_t)d * row_bytes, srow, (uint32_t)row_bytes);
+            if (bulk_scales)
+                bulk_store(static_cast<uint8_t *>(scales) + (size_t)d * scale_bytes, sscale,
+                           (uint32_t)scale_bytes);
+        }
+        bulk_commit();
+    }
+    // remaining scale rows: 4-byte words by the other threads
+    if (Q != EP_QUANT_NONE && !bulk_scales) {
+        const int words = scale_bytes >> 2;
+        for (int j = threadIdx.x; j < K * words; j += blockDim.x) {
+            const int k = j / words, wd = j - k * words;
+            const int d = sdst[k];
+            if (d >= 0)
+                reinterpret_cast<uint32_t *>(scales)[(size_t)d * words + wd] =
+                    reinterpret_cast<const uint32_t *>(sscale)[wd];
+        }
+    }
+    if (row_w && threadIdx.x < K) {
+        const int d = sdst[threadIdx.x];
+        if (d >= 0) row_w[d] = __ldg(topk_w + (size_t)t * K + threadIdx.x);
+    }
+    if (threadIdx.x == 0) bulk_wait_read();  // staging must outlive the bulk reads
+}
+
+template <int Q>
+cudaError_t launch_q(const ep_layout_t &L, const void *x, int H, void *out_rows,
+                     void *out_scales, const float *topk_w, float *row_w, cudaStream_t stream) {
+    const int G = H / 128;
+    const int row_bytes = Q == EP_QUANT_NONE ? 2 * H : H;
+    const int scale_bytes = Q == EP_QUANT_FP8_F32 ? 4 * G : Q == EP_QUANT_FP8_UE8M0 ? ((G + 3) / 4) * 4 : 0;
+    const size_t smem = (size_t)row_bytes + (size_t)scale_bytes;
+    // one slot per 16 elements (FP8) or per 16-byte chunk (bf16), up to 512 threads
+    int slots = Q == EP_QUANT_NONE ? H / 8 : G * 8;
+    int threads = ((slots + 31) / 32) * 32;
+    if (threads > kMaxThreads) threads = kMaxThreads;
+    if (threads < 64) threads = 64;  // K <= 32 threads read dst_row; scale pads
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(dispatch_kernel<Q>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    const bool bulk_scales = Q == EP_QUANT_FP8_F32 && (scale_bytes % 16) == 0 &&
+                             (reinterpret_cast<uintptr_t>(out_scales) % 16) == 0;
+    // programmatic dependent of the layout: x is loaded and quantised while
+    // the layout kernels finish
+    return launch_kernel(dispatch_kernel<Q>, L.num_tokens, threads, smem, stream, true,
+                         static_cast<const uint16_t *>(x), L.num_topk, H, L.dst_row,
+                         static_cast<uint8_t *>(out_rows), out_scales, topk_w, row_w,
+                         bulk_scales);
 }
 
 }  // namespace
@@ -141,26 +196,15 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t launch_dispatch(const ep_layout_t &L, const void *x, int H, ep_quant_t quant,
                             void *out_rows, void *out_scales, const float *topk_w,
                             float *row_w, cudaStream_t stream) {
-    const int T = L.num_tokens, K = L.num_topk;
-    if (T == 0) return cudaSuccess;
-    const uint16_t *xb = static_cast<const uint16_t *>(x);
-    if (quant == EP_QUANT_NONE) {
-        const long long n = (long long)T * (H / 8);
-        const long long blocks = (n + kThreads - 1) / kThreads;
-        dispatch_bf16_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(
-            xb, K, H, n, L.dst_row, static_cast<uint16_t *>(out_rows), topk_w, row_w);
-    } else {
-        const long long n = (long long)T * (H / 128);
-        const long long blocks = (n * 8 + kThreads - 1) / kThreads;
-        uint8_t *o = static_cast<uint8_t *>(out_rows);
-        if (quant == EP_QUANT_FP8_F32)
-            dispatch_fp8_kernel<EP_QUANT_FP8_F32><<<(unsigned)blocks, kThreads, 0, stream>>>(
-                xb, K, H, n, L.dst_row, o, out_scales, topk_w, row_w);
-        else
-            dispatch_fp8_kernel<EP_QUANT_FP8_UE8M0><<<(unsigned)blocks, kThreads, 0, stream>>>(
-                xb, K, H, n, L.dst_row, o, out_scales, topk_w, row_w);
+    if (L.num_tokens == 0) return cudaSuccess;
+    switch (quant) {
+        case EP_QUANT_NONE:
+            return launch_q<EP_QUANT_NONE>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+        case EP_QUANT_FP8_F32:
+            return launch_q<EP_QUANT_FP8_F32>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+        default:
+            return launch_q<EP_QUANT_FP8_UE8M0>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace ep

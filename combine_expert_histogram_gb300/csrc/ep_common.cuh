@@ -87,11 +87,33 @@ __device__ __forceinline__ void block_exclusive_scan(int n, F value, int32_t *ou
 // Per-device properties, cached on first use (host side).
 int sm_count();
 
+// Launch with cudaLaunchKernelEx; `programmatic` lets the kernel start while the
+// previous kernel on the stream still runs (programmatic dependent launch): it
+// must then call griddepcontrol.wait before touching that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*k)(KArgs...), int grid, int threads, size_t smem,
+                          cudaStream_t stream, bool programmatic, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 // Internal launchers (one translation unit each).  They assume arguments were
 // validated by the C ABI layer in abi.cu.
 struct LayoutPlan {
+    int threads;      // threads of the assign kernel's CTAs
+    int chunk;        // entries per warp per pass
+    int passes;       // passes per tile
     int tiles;        // tiles of topk_idx entries (CTAs that assign slots)
-    int tile;         // entries per tile, a multiple of 512
+    int tile;         // entries per tile
     int grid;         // CTAs of the assign kernel (>= tiles; extra CTAs fill padding)
     size_t smem;      // dynamic shared memory of the assign kernel
     size_t ws_bytes;  // scratch: tiles x E int32 per-tile histograms (0 when tiles == 1)

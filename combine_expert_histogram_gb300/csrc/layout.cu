@@ -7,40 +7,43 @@
 // (ElasticBuffer) MoE A2A backend", section "Supported scope".
 //
 // Design (deterministic, no global atomics on slot order; latency-bound, so
-// the goal is short dependency chains and every SM busy):
-//   * the T*K entries are cut into tiles of 2048 entries (more for huge
-//     inputs), one CTA of 256 threads per tile; warp w owns a contiguous
-//     chunk of its tile and lane l holds entries chunk + 32r + l, r < rounds,
-//     in registers (all loads issued up front);
+// the goal is short dependency chains and many warps):
+//   * the T*K entries are cut into tiles; warp w of a tile's CTA owns a
+//     contiguous chunk of at most 256 entries, lane l holds entries
+//     chunk + 32r + l in registers (all loads issued up front);
 //   * lanes holding the same expert in a round find each other with
 //     ceil(log2(E+1)) independent __ballot_sync's (one per bit of the id);
 //     the mask is kept per round and reused for ranking;
-//   * tile_hist_kernel (only with >= 2 tiles) writes each tile's expert
-//     histogram to the scratch workspace [tiles][E];
-//   * assign_kernel: every CTA sums the workspace columns (independent L2
-//     loads) into the expert totals and its tile's base, scans the padded
-//     counts, turns per-warp histograms into per-warp starting slots, and
-//     gives each entry slot = warp base + #lower lanes with the same expert.
-//     That order is exactly ascending (token, k);
-//   * extra CTAs (masked layouts with row_src) only write -1 into row_src for
-//     empty slots.
+//   * up to 8192 entries (decode batches) one 1024-thread CTA does everything
+//     in one kernel; above that, tiles of 2048 entries on 256-thread CTAs:
+//     tile_hist_kernel writes each tile's expert histogram to the scratch
+//     workspace [tiles][E], then assign_kernel (launched as a programmatic
+//     dependent, so its loads and ballots overlap tile_hist) waits for it and
+//     sums the workspace columns into the expert totals and its tile's base;
+//   * assign_kernel scans the padded counts, turns per-warp histograms into
+//     per-warp starting slots and gives each entry
+//     slot = warp base + #lower lanes with the same expert: exactly ascending
+//     (token, k) order;
+//   * extra CTAs (masked layouts with row_src) only count the experts with
+//     shared-memory atomics and write -1 into row_src for empty slots.
 #include "ep_common.cuh"
 
 namespace ep {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kRounds = 8;                    // 32-entry rounds per warp chunk
-constexpr int kTile = kThreads * kRounds;     // 2048 entries
-constexpr int kMaxBits = 11;                  // ids 0..1024 (1024 = "no expert")
+constexpr int kRounds = 8;       // max 32-entry rounds per warp chunk
+constexpr int kChunk = 32 * kRounds;
 constexpr int kFillCtas = 128;
-constexpr int kSumChunk = 16;                 // workspace loads in flight per thread
+constexpr int kSumChunk = 16;    // workspace loads in flight per thread
+constexpr int kSmallThreads = 1024;                     // single-tile CTA
+constexpr int kTileThreads = 256;                       // multi-tile CTAs
+constexpr int kSmallMax = kSmallThreads / 32 * kChunk;  // 8192 entries
+constexpr int kTile = kTileThreads / 32 * kChunk;       // 2048 entries
 
 __host__ __device__ inline int round_up_pow2(int v, int a) { return (v + a - 1) & ~(a - 1); }
 
-// A warp chunk, kRounds entries per lane: ids (invalid ones mapped to E),
-// peer masks (lanes with the same id this round) and the bad-id flags.
+// A warp chunk, up to kRounds entries per lane: ids (invalid ones mapped to
+// E), peer masks (lanes with the same id this round) and the bad-id flags.
 struct Chunk {
     int ev[kRounds];
     unsigned peers[kRounds];
@@ -64,11 +67,12 @@ __device__ __forceinline__ void load_chunk(const int32_t *__restrict__ idx, int 
     }
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
-        const int v = c.ev[r];
-        unsigned m = kFullMask;
-#pragma unroll
-        for (int b = 0; b < kMaxBits; ++b) {
-            if (b < nbits) {  // warp-uniform
+        unsigned m = 0;
+        if (c0 + r * 32 < c1) {  // warp-uniform: rounds past the chunk stay empty
+            const int v = c.ev[r];
+            m = kFullMask;
+#pragma unroll 1
+            for (int b = 0; b < nbits; ++b) {  // warp-uniform trip count; kept rolled (code size)
                 const unsigned bit = (v >> b) & 1u;
                 const unsigned bal = __ballot_sync(kFullMask, bit);
                 m &= bit ? bal : ~bal;
@@ -80,11 +84,17 @@ __device__ __forceinline__ void load_chunk(const int32_t *__restrict__ idx, int 
 
 __device__ __forceinline__ int id_bits(int E) { return 32 - __clz(E); }  // E itself must fit
 
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kTileThreads)
     tile_hist_kernel(const int32_t *__restrict__ idx, int TK, int E, int tile,
                      int32_t *__restrict__ ws, int32_t *__restrict__ status) {
+    pdl_launch_dependents();  // the assign kernel may start its own loads now
     extern __shared__ int32_t hist[];  // [E]
-    for (int e = threadIdx.x; e < E; e += kThreads) hist[e] = 0;
+    for (int e = threadIdx.x; e < E; e += kTileThreads) hist[e] = 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int start = blockIdx.x * tile;
     const int end = min(TK, start + tile);
@@ -92,8 +102,8 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();  // hist zeroed
     // tiles larger than kTile (huge inputs) are walked in kTile-sized passes
     for (int base = start; base < end; base += kTile) {  // block-uniform
-        const int c0 = base + warp * kRounds * 32;
-        const int c1 = min(end, c0 + kRounds * 32);
+        const int c0 = base + warp * kChunk;
+        const int c1 = min(end, c0 + kChunk);
         load_chunk(idx, c0, c1, E, id_bits(E), c);
 #pragma unroll
         for (int r = 0; r < kRounds; ++r) {
@@ -102,49 +112,78 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kThreads) ws[(size_t)blockIdx.x * E + e] = hist[e];
-    // The assign kernel runs after this one on the stream and raises errors.
+    for (int e = threadIdx.x; e < E; e += kTileThreads) ws[(size_t)blockIdx.x * E + e] = hist[e];
+    // The assign kernel raises errors only after waiting for this kernel.
     if (blockIdx.x == 0 && threadIdx.x == 0) *status = EP_OK;
 }
 
 struct AssignArgs {
     const int32_t *idx;
     int TK, E, R, masked, align, cap;
+    int chunk;   // entries per warp per pass (multiple of 32, <= kChunk)
+    int passes;  // passes per tile
     int tile, tiles;
     const int32_t *ws;  // [tiles][E]; unused when tiles == 1
     int32_t *dst_row, *row_src, *count, *offset, *rank_rows, *status;
 };
 
-__global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
+template <int NT>
+__global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
+    constexpr int kWarps = NT / 32;
     extern __shared__ int32_t sm[];
     const int E = a.E;
-    int32_t *wh = sm;                  // [passes][kWarps][E]: per-warp counts, then slot bases
-    const int passes = a.tile / kTile;
+    const int passes = a.passes;
+    int32_t *wh = sm;                         // [passes][kWarps][E]: per-warp counts, then slot bases
     int32_t *tot = wh + passes * kWarps * E;  // [E] expert histogram
     int32_t *off = tot + E;                   // [E+1] first row of each expert
+    int32_t *cum = off + E + 1;               // [E+1] unpadded prefix (rank_rows)
     __shared__ int32_t scan_tmp[kWarps];
+
+    pdl_launch_dependents();  // dispatch may start loading and quantising x now
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool assigns = blockIdx.x < a.tiles;
-    const int tile_id = assigns ? blockIdx.x : 0;
+    const int tile_id = blockIdx.x;
     const int start = tile_id * a.tile;
     const int end = min(a.TK, start + a.tile);
-    const bool need_hist = assigns || a.tiles == 1;
     const int nbits = id_bits(E);
+    const int pass_len = kWarps * a.chunk;
 
-    // With one tile this is the only layout kernel: reset the status word
-    // before any error of this CTA is raised (ordered by the barriers below).
-    if (a.tiles == 1 && blockIdx.x == 0 && threadIdx.x == 0) *a.status = EP_OK;
-    for (int j = threadIdx.x; j < passes * kWarps * E; j += kThreads) wh[j] = 0;
+    if (!assigns) {
+        // Fill CTA (masked layouts with row_src): only the expert counts are
+        // needed, in any order; masked offsets are e*cap, so no scan either.
+        if (a.tiles == 1) {
+            for (int e = threadIdx.x; e < E; e += NT) tot[e] = 0;
+            __syncthreads();
+            for (int i = threadIdx.x; i < a.TK; i += NT) {
+                const int e = __ldg(a.idx + i);
+                if (e >= 0 && e < E) atomicAdd(&tot[e], 1);
+            }
+        } else {
+            pdl_wait();
+            for (int e = threadIdx.x; e < E; e += NT) {
+                int total = 0;
+                for (int b = 0; b < a.tiles; ++b) total += __ldcg(a.ws + (size_t)b * E + e);
+                tot[e] = total;
+            }
+        }
+        __syncthreads();
+        for (int e = blockIdx.x; e < E; e += gridDim.x)
+            for (int r = e * a.cap + min(tot[e], a.cap) + (int)threadIdx.x; r < (e + 1) * a.cap; r += NT)
+                a.row_src[r] = -1;
+        return;
+    }
+
+    for (int j = threadIdx.x; j < passes * kWarps * E; j += NT) wh[j] = 0;
     __syncthreads();
 
-    // 1. per-(pass, warp) expert histogram of this tile; chunks stay in registers
-    //    only for single-pass tiles (the common case), else they are reloaded.
+    // 1. per-(pass, warp) expert histogram of this tile; chunks stay in
+    //    registers for single-pass tiles (the common case), else are reloaded.
     Chunk c;
-    if (need_hist) {
+    {
         for (int p = 0; p < passes; ++p) {
-            const int c0 = start + p * kTile + warp * kRounds * 32;
-            const int c1 = min(end, c0 + kRounds * 32);
+            const int c0 = start + p * pass_len + warp * a.chunk;
+            const int c1 = min(end, c0 + a.chunk);
             load_chunk(a.idx, c0, c1, E, nbits, c);
             int32_t *row = wh + (p * kWarps + warp) * E;
 #pragma unroll
@@ -155,10 +194,14 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
             }
         }
     }
+    // Everything below reads the histogram kernel's workspace or writes the
+    // status word it resets: wait for it (a no-op without a programmatic edge).
+    pdl_wait();
+    if (a.tiles == 1 && blockIdx.x == 0 && threadIdx.x == 0) *a.status = EP_OK;
     __syncthreads();
 
     // 2. expert totals and this tile's base; per-warp counts -> starting slots
-    for (int e = threadIdx.x; e < E; e += kThreads) {
+    for (int e = threadIdx.x; e < E; e += NT) {
         int total = 0, base = 0;
         if (a.tiles == 1) {
             for (int j = 0; j < passes * kWarps; ++j) total += wh[j * E + e];
@@ -176,7 +219,7 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
             }
         }
         tot[e] = total;
-        if (assigns) {
+        {
             int run = base;
             for (int j = 0; j < passes * kWarps; ++j) {  // (pass, warp) order = entry order
                 const int cnt = wh[j * E + e];
@@ -189,30 +232,29 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
 
     // 3. padded exclusive scan (contiguous) or fixed stride (masked)
     const int align = a.align, cap = a.cap, masked = a.masked;
-    block_exclusive_scan<kThreads>(
+    block_exclusive_scan<NT>(
         E, [&](int e) { return masked ? cap : round_up_pow2(tot[e], align); }, off, scan_tmp);
 
     if (blockIdx.x == 0) {
-        for (int e = threadIdx.x; e < E; e += kThreads) {
+        if (a.rank_rows)  // rows of rank r = unpadded prefix difference over its experts
+            block_exclusive_scan<NT>(E, [&](int e) { return tot[e]; }, cum, scan_tmp);
+        for (int e = threadIdx.x; e < E; e += NT) {
             a.count[e] = tot[e];
             a.offset[e] = off[e];
         }
         if (threadIdx.x == 0) a.offset[E] = off[E];
         if (a.rank_rows) {
             const int per = E / a.R;
-            for (int r = threadIdx.x; r < a.R; r += kThreads) {
-                int s = 0;
-                for (int e = r * per; e < (r + 1) * per; ++e) s += tot[e];
-                a.rank_rows[r] = s;
-            }
+            for (int r = threadIdx.x; r < a.R; r += NT)
+                a.rank_rows[r] = cum[(r + 1) * per] - cum[r * per];
         }
     }
 
     // 4. stable slots: warp base + rank among lower lanes with the same expert
-    if (assigns) {
+    {
         for (int p = 0; p < passes; ++p) {
-            const int c0 = start + p * kTile + warp * kRounds * 32;
-            const int c1 = min(end, c0 + kRounds * 32);
+            const int c0 = start + p * pass_len + warp * a.chunk;
+            const int c1 = min(end, c0 + a.chunk);
             if (passes > 1) load_chunk(a.idx, c0, c1, E, nbits, c);
             int32_t *row = wh + (p * kWarps + warp) * E;
 #pragma unroll
@@ -243,12 +285,13 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
         }
     }
 
-    // 5. row_src = -1 on padding rows (contiguous) and empty slots (masked)
+    // 5. row_src = -1 on padding rows (contiguous) and empty slots (masked);
+    //    fill CTAs, when present, took the other experts
     if (a.row_src) {
         for (int e = blockIdx.x; e < E; e += gridDim.x) {
             const int r0 = off[e] + (masked ? min(tot[e], cap) : tot[e]);
             const int r1 = masked ? off[e] + cap : off[e + 1];
-            for (int r = r0 + (int)threadIdx.x; r < r1; r += kThreads) a.row_src[r] = -1;
+            for (int r = r0 + (int)threadIdx.x; r < r1; r += NT) a.row_src[r] = -1;
         }
     }
 }
@@ -258,22 +301,38 @@ __global__ void __launch_bounds__(kThreads) assign_kernel(AssignArgs a) {
 LayoutPlan layout_plan(const ep_layout_t &L) {
     LayoutPlan p{};
     const long long TK = (long long)L.num_tokens * L.num_topk;
-    // tiles of kTile entries; inputs beyond 128 tiles grow the tile by whole
-    // kTile passes instead, which bounds the workspace and the column sums
-    long long tiles = (TK + kTile - 1) / kTile;
-    if (tiles < 1) tiles = 1;
-    int passes = 1;
-    if (tiles > 128) {
-        passes = (int)((tiles + 127) / 128);
-        tiles = (TK + (long long)kTile * passes - 1) / ((long long)kTile * passes);
+    int warps;
+    if (TK <= kSmallMax) {
+        // one 1024-thread CTA; chunks as short as possible so all warps share the work
+        p.threads = kSmallThreads;
+        warps = kSmallThreads / 32;
+        p.tiles = 1;
+        p.passes = 1;
+        const long long per_warp = (TK + warps - 1) / warps;
+        p.chunk = (int)((per_warp + 31) / 32 * 32);
+        if (p.chunk == 0) p.chunk = 32;
+        p.tile = p.chunk * warps;
+    } else {
+        // tiles of kTile entries; beyond 128 tiles the tile grows in whole
+        // kTile passes instead, which bounds the workspace and the column sums
+        p.threads = kTileThreads;
+        warps = kTileThreads / 32;
+        p.chunk = kChunk;
+        long long tiles = (TK + kTile - 1) / kTile;
+        p.passes = 1;
+        if (tiles > 128) {
+            p.passes = (int)((tiles + 127) / 128);
+            tiles = (TK + (long long)kTile * p.passes - 1) / ((long long)kTile * p.passes);
+        }
+        p.tiles = (int)tiles;
+        p.tile = kTile * p.passes;
     }
-    p.tiles = (int)tiles;
-    p.tile = kTile * passes;
     const bool fill = L.kind == EP_LAYOUT_MASKED && L.row_src != nullptr;
     p.grid = p.tiles;
     if (fill && p.grid < kFillCtas) p.grid = L.num_experts < kFillCtas ? L.num_experts : kFillCtas;
     if (p.grid < p.tiles) p.grid = p.tiles;
-    p.smem = sizeof(int32_t) * ((size_t)passes * kWarps * L.num_experts + 2 * (size_t)L.num_experts + 1);
+    p.smem = sizeof(int32_t) *
+             ((size_t)p.passes * warps * L.num_experts + 3 * (size_t)L.num_experts + 2);
     p.ws_bytes = p.tiles > 1 ? sizeof(int32_t) * (size_t)p.tiles * L.num_experts : 0;
     return p;
 }
@@ -283,17 +342,6 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     const LayoutPlan p = layout_plan(L);
     const int TK = L.num_tokens * L.num_topk;
     const int E = L.num_experts;
-    if (p.tiles > 1) {
-        tile_hist_kernel<<<p.tiles, kThreads, sizeof(int32_t) * E, stream>>>(
-            topk_idx, TK, E, p.tile, workspace, L.status);
-        cudaError_t err = cudaGetLastError();
-        if (err != cudaSuccess) return err;
-    }
-    if (p.smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(
-            assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-        if (err != cudaSuccess) return err;
-    }
     AssignArgs a;
     a.idx = topk_idx;
     a.TK = TK;
@@ -302,6 +350,8 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     a.masked = L.kind == EP_LAYOUT_MASKED;
     a.align = a.masked ? 1 : L.align;
     a.cap = a.masked ? L.capacity : 0;
+    a.chunk = p.chunk;
+    a.passes = p.passes;
     a.tile = p.tile;
     a.tiles = p.tiles;
     a.ws = workspace;
@@ -311,8 +361,27 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     a.offset = L.expert_offset;
     a.rank_rows = L.rank_rows;
     a.status = L.status;
-    assign_kernel<<<p.grid, kThreads, p.smem, stream>>>(a);
-    return cudaGetLastError();
+    cudaError_t err;
+    if (p.threads == kSmallThreads) {
+        if (p.smem > 48 * 1024) {
+            err = cudaFuncSetAttribute(assign_kernel<kSmallThreads>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+            if (err != cudaSuccess) return err;
+        }
+        // first kernel of the layout: an ordinary launch, ordered after all prior work
+        return launch_kernel(assign_kernel<kSmallThreads>, p.grid, kSmallThreads, p.smem, stream,
+                             false, a);
+    }
+    err = launch_kernel(tile_hist_kernel, p.tiles, kTileThreads, sizeof(int32_t) * E, stream,
+                        false, topk_idx, TK, E, p.tile, workspace, L.status);
+    if (err != cudaSuccess) return err;
+    if (p.smem > 48 * 1024) {
+        err = cudaFuncSetAttribute(assign_kernel<kTileThreads>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+        if (err != cudaSuccess) return err;
+    }
+    return launch_kernel(assign_kernel<kTileThreads>, p.grid, kTileThreads, p.smem, stream, true,
+                         a);
 }
 
 }  // namespace ep

@@ -87,8 +87,11 @@ def check_layout(w, case, g, orc=None):
     return ref
 
 
-def check_dispatch(w, case, g, ref, sample_tokens=None, seed=0, orc=None):
+def check_dispatch(w, case, g, ref, sample_tokens=None, seed=0, orc=None, check_row_w=True,
+                   check_empty=None):
     """Bit-exact rows/scales/row_w; sentinel kept on rows the layout leaves empty."""
+    if check_empty is None:
+        check_empty = check_row_w
     orc = orc or oracle.default()
     T, K = case["idx"].shape
     if T == 0:
@@ -115,8 +118,11 @@ def check_dispatch(w, case, g, ref, sample_tokens=None, seed=0, orc=None):
     if w.quant != "none":
         gs = g["out_scales"].index_select(0, sel).cpu().numpy()
         assert np.array_equal(gs.view(np.uint32), o_sc[osel].view(np.uint32)), "scales differ"
-    assert np.array_equal(g["row_w"].index_select(0, sel).cpu().numpy().view(np.uint32),
-                          o_w[osel].view(np.uint32))
+    if check_row_w:
+        assert np.array_equal(g["row_w"].index_select(0, sel).cpu().numpy().view(np.uint32),
+                              o_w[osel].view(np.uint32))
+    if not check_empty:
+        return
     # rows no entry maps to keep the sentinel (padding and empty slots)
     rows = ref["rows"]
     used = torch.zeros(max(rows, 1), dtype=torch.bool, device=g["out_rows"].device)
