@@ -25,7 +25,7 @@ HDR = os.path.join(_HERE, "oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 OK, CAPACITY, BAD_EXPERT_ID = 0, 2, 3
-QUANT = {"none": 0, "fp8_f32": 1, "fp8_ue8m0": 2}
+QUANT = {"none": 0, "fp8_f32": 1, "fp8_ue8m0": 2, "mxfp8": 3}
 
 GCC_FLAGS = ["-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
 
@@ -61,7 +61,9 @@ def rows_capacity(T, K, E, align, layout, cap=0):
 def scale_cols(H: int, quant: str) -> int:
     """fp32 / int32 scale words per row."""
     G = H // 128
-    return G if quant == "fp8_f32" else (G + 3) // 4 if quant == "fp8_ue8m0" else 0
+    if quant in ("fp8_f32", "mxfp8"):
+        return G  # fp32 words, or 4 E8M0 bytes per int32 word
+    return (G + 3) // 4 if quant == "fp8_ue8m0" else 0
 
 
 class Oracle:
@@ -82,6 +84,8 @@ class Oracle:
         L.orc_quant_group_f32.argtypes = [P, I, P, P]
         L.orc_quant_group_ue8m0.restype = None
         L.orc_quant_group_ue8m0.argtypes = [P, I, P, P]
+        L.orc_quant_block_mx.restype = None
+        L.orc_quant_block_mx.argtypes = [P, I, P, P]
         L.orc_layout.restype = I
         L.orc_layout.argtypes = [P, I, I, I, I, I, I, I, P, P, P, P, P]
         L.orc_dispatch.restype = None
@@ -117,7 +121,7 @@ class Oracle:
         return float(self.lib.orc_e4m3_decode(int(c)))
 
     def quant_group(self, x_bits: np.ndarray, mode: str):
-        """Quantise one group: (q uint8 [n], fp32 scale | UE8M0 exponent byte)."""
+        """Quantise one group: (q uint8 [n], fp32 scale | UE8M0 / E8M0 byte)."""
         x = np.ascontiguousarray(x_bits, dtype=np.uint16)
         q = np.zeros(x.size, dtype=np.uint8)
         if mode == "fp8_f32":
@@ -125,7 +129,10 @@ class Oracle:
             self.lib.orc_quant_group_f32(_p(x), x.size, _p(q), _p(s))
             return q, float(s[0])
         e = np.zeros(1, dtype=np.uint8)
-        self.lib.orc_quant_group_ue8m0(_p(x), x.size, _p(q), _p(e))
+        if mode == "mxfp8":
+            self.lib.orc_quant_block_mx(_p(x), x.size, _p(q), _p(e))
+        else:
+            self.lib.orc_quant_group_ue8m0(_p(x), x.size, _p(q), _p(e))
         return q, int(e[0])
 
     # --------------------------------------------------------------- layout
@@ -160,7 +167,7 @@ class Oracle:
             sc = None
         else:
             out = np.full((rows, H), fill, dtype=np.uint8)
-            dt = np.float32 if quant == "fp8_f32" else np.int32
+            dt = np.float32 if quant == "fp8_f32" else np.int32  # mxfp8: 4 E8M0 bytes per word
             sc = np.zeros((rows, scale_cols(H, quant)), dtype=dt)
         row_w = w = None
         if topk_w is not None:

@@ -105,6 +105,28 @@ void orc_quant_group_ue8m0(const uint16_t *x, int n, uint8_t *q, uint8_t *exp_by
     *exp_byte = (uint8_t)e;
 }
 
+/* MXFP8 (OCP Microscaling Formats (MX) v1.0, "conversion from a vector of
+ * scalars"): one shared scale per block of 32 elements, X = 2^(floor(log2
+ * amax) - 8), 8 being the exponent of E4M3's largest normal (448 = 1.75*2^8);
+ * elements q = E4M3_rne_satfinite(x / X).  X is stored as an E8M0 byte (bias
+ * 127) and clamped at its smallest value 2^-127 (byte 0), which also covers
+ * all-zero and subnormal blocks.  For a normal amax, floor(log2 amax) is its
+ * unbiased exponent, so the byte is max(0, biased_exponent(amax) - 8), and
+ * x / X = x * 2^(127 - byte) is a multiply by a power of two. */
+void orc_quant_block_mx(const uint16_t *x, int n, uint8_t *q, uint8_t *scale_byte) {
+    float amax = group_amax(x, n);
+    int e = 0; /* biased exponent of amax; 0 for zero and subnormals */
+    if (amax >= ldexpf(1.0f, -126)) {
+        int ex;
+        frexpf(amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+        e = ex - 1 + 127;
+    }
+    int byte = e - 8 > 0 ? e - 8 : 0;
+    float inv = ldexpf(1.0f, 127 - byte);
+    for (int i = 0; i < n; ++i) q[i] = orc_e4m3_encode(orc_bf16_to_float(x[i]) * inv);
+    *scale_byte = (uint8_t)byte;
+}
+
 /* ---------------------------------------------------------------- layout */
 
 static int round_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -187,6 +209,8 @@ int orc_layout(const int32_t *topk_idx, int T, int K, int E, int R, int masked,
  *   ORC_Q_FP8_UE8M0: E4M3 bytes [rows, H]; scale bytes [rows, 4*ceil(G/4)],
  *                    byte g = exponent of group g (byte g%4 of little-endian
  *                    int32 word g/4), unused trailing bytes = 127 (2^0).
+ *   ORC_Q_MXFP8:     E4M3 bytes [rows, H]; E8M0 bytes [rows, H/32], byte b =
+ *                    scale of elements 32b..32b+31 (H/128 int32 words).
  * row_w[dst] = topk_w[t*K+k] when both are given. */
 void orc_dispatch(const uint16_t *x, int T, int K, int H, int quant,
                   const int32_t *dst_row, void *out_rows, void *out_scales,
@@ -196,6 +220,7 @@ void orc_dispatch(const uint16_t *x, int T, int K, int H, int quant,
     uint8_t *q = (uint8_t *)malloc((size_t)(H > 0 ? H : 1));
     float *sc = (float *)malloc(sizeof(float) * (size_t)(G > 0 ? G : 1));
     uint8_t *eb = (uint8_t *)malloc((size_t)(4 * P > 0 ? 4 * P : 1));
+    uint8_t *mx = (uint8_t *)malloc((size_t)(H / 32 > 0 ? H / 32 : 1));
     for (int t = 0; t < T; ++t) {
         const uint16_t *xr = x + (size_t)t * H;
         if (quant == ORC_Q_FP8_F32) {
@@ -203,6 +228,8 @@ void orc_dispatch(const uint16_t *x, int T, int K, int H, int quant,
         } else if (quant == ORC_Q_FP8_UE8M0) {
             for (int b = 0; b < 4 * P; ++b) eb[b] = 127;
             for (int g = 0; g < G; ++g) orc_quant_group_ue8m0(xr + g * 128, 128, q + g * 128, &eb[g]);
+        } else if (quant == ORC_Q_MXFP8) {
+            for (int b = 0; b < H / 32; ++b) orc_quant_block_mx(xr + b * 32, 32, q + b * 32, &mx[b]);
         }
         for (int k = 0; k < K; ++k) {
             int dst = dst_row[t * K + k];
@@ -213,8 +240,10 @@ void orc_dispatch(const uint16_t *x, int T, int K, int H, int quant,
                 memcpy((uint8_t *)out_rows + (size_t)dst * H, q, (size_t)H);
                 if (quant == ORC_Q_FP8_F32)
                     memcpy((float *)out_scales + (size_t)dst * G, sc, sizeof(float) * (size_t)G);
-                else
+                else if (quant == ORC_Q_FP8_UE8M0)
                     memcpy((uint8_t *)out_scales + (size_t)dst * 4 * P, eb, (size_t)(4 * P));
+                else
+                    memcpy((uint8_t *)out_scales + (size_t)dst * (H / 32), mx, (size_t)(H / 32));
             }
             if (topk_w && row_w) row_w[dst] = topk_w[t * K + k];
         }
@@ -222,6 +251,7 @@ void orc_dispatch(const uint16_t *x, int T, int K, int H, int quant,
     free(q);
     free(sc);
     free(eb);
+    free(mx);
 }
 
 /* --------------------------------------------------------------- combine */
@@ -257,7 +287,8 @@ int orc_masked_repack(const void *rows, const void *row_scales, int H, int quant
     size_t row_bytes = quant == ORC_Q_NONE ? 2 * (size_t)H : (size_t)H;
     int G = H / 128;
     size_t scale_bytes = quant == ORC_Q_FP8_F32 ? 4 * (size_t)G
-                         : quant == ORC_Q_FP8_UE8M0 ? 4 * (size_t)((G + 3) / 4) : 0;
+                         : quant == ORC_Q_FP8_UE8M0 ? 4 * (size_t)((G + 3) / 4)
+                         : quant == ORC_Q_MXFP8 ? (size_t)(H / 32) : 0;
     for (int e = 0; e < E; ++e) {
         int n = count[e];
         if (n > cap) {

@@ -13,7 +13,10 @@
  *     "Add DeepEPv2 (ElasticBuffer) MoE A2A backend", section "Supported scope");
  *   - dispatch: row scatter fused with dynamic 1x128 FP8-E4M3 quantisation with
  *     fp32 or packed UE8M0 scales (same PR, section "Implementation"; SGLang
- *     discussion "deepep v2 support?", the 128x128 blockwise FP8 gate);
+ *     discussion "deepep v2 support?", the 128x128 blockwise FP8 gate), or
+ *     1x32 MXFP8 (the same discussion's "1x32 MXFP8 ... with dynamic
+ *     activation scaling", with the OCP Microscaling Formats (MX) v1.0
+ *     conversion rule for the shared scale);
  *   - combine: top-k weighted reduction back to token order (vLLM
  *     tools/ep_kernels commit message, "weighted reduction in combine");
  *   - masked repack: contiguous expert segments -> [E, cap, H] slab.
@@ -42,6 +45,7 @@ extern "C" {
 #define ORC_Q_NONE 0      /* bf16 rows */
 #define ORC_Q_FP8_F32 1   /* E4M3 rows + fp32 scale per 1x128 group */
 #define ORC_Q_FP8_UE8M0 2 /* E4M3 rows + one UE8M0 byte per group, 4 per int32 */
+#define ORC_Q_MXFP8 3     /* E4M3 rows + one E8M0 byte per 32 elements (OCP MX) */
 
 uint16_t orc_bf16_round(float f);
 float orc_bf16_to_float(uint16_t b);
@@ -50,6 +54,7 @@ double orc_e4m3_decode(uint8_t code);
 
 void orc_quant_group_f32(const uint16_t *x, int n, uint8_t *q, float *scale);
 void orc_quant_group_ue8m0(const uint16_t *x, int n, uint8_t *q, uint8_t *exp_byte);
+void orc_quant_block_mx(const uint16_t *x, int n, uint8_t *q, uint8_t *scale_byte);
 
 int orc_layout(const int32_t *topk_idx, int T, int K, int E, int R, int masked,
                int align, int cap, int32_t *count, int32_t *offset,

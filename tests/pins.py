@@ -211,6 +211,29 @@ def pin_quant_ue8m0(orc, rng):
         assert np.array_equal(q, e4m3_nearest(v))
 
 
+def pin_quant_mx(orc, rng):
+    """OCP MX conversion: X = 2^(floor(log2 amax) - 8), so amax / X lies in
+    [256, 512) for every normal amax; E8M0 byte = log2 X + 127, clamped at 0."""
+    blocks = [b[:32] for b in _groups(rng)] + [b[32:64] for b in _groups(rng, 24)]
+    tiny = torch_bf16_bits(np.full(32, 2.0 ** -130, dtype=np.float32))  # subnormal block
+    blocks.append(tiny)
+    for xb in blocks:
+        x = bf16_bits_to_f32(xb).astype(np.float64)
+        q, byte = orc.quant_group(xb, "mxfp8")
+        amax = float(np.abs(x).max())
+        if amax >= 2.0 ** -126:
+            _, ex = math.frexp(amax)  # amax = f * 2^ex, f in [0.5, 1)
+            shared = ex - 1 - 8
+            assert byte == max(0, shared + 127), (amax, byte)
+            X = math.ldexp(1.0, byte - 127)
+            if byte > 0:
+                assert 256.0 <= amax / X < 512.0
+        else:
+            assert byte == 0  # zero and subnormal blocks: smallest E8M0 scale
+        X = math.ldexp(1.0, byte - 127)
+        assert np.array_equal(q, e4m3_nearest(x / X))  # saturates above 448
+
+
 # ------------------------------------------------------------------ layout
 def _check_layout(orc, idx, E, kind, align, cap, R):
     T, K = idx.shape
@@ -280,7 +303,7 @@ def pin_layout_bad_ids(orc, rng):
 # ---------------------------------------------------------------- dispatch
 def pin_dispatch(orc, rng):
     for quant, H in (("none", 256), ("fp8_f32", 384), ("fp8_ue8m0", 128), ("fp8_ue8m0", 384),
-                     ("fp8_ue8m0", 7168), ("fp8_f32", 7168)):
+                     ("fp8_ue8m0", 7168), ("fp8_f32", 7168), ("mxfp8", 128), ("mxfp8", 640)):
         T, K, E = 9, 3, 5
         idx = rng.integers(-1, E, size=(T, K)).astype(np.int32)
         w = rng.random((T, K)).astype(np.float32)
@@ -299,6 +322,13 @@ def pin_dispatch(orc, rng):
                 assert roww[r] == w[t, k]
                 if quant == "none":
                     assert np.array_equal(out[r], x[t])
+                    continue
+                if quant == "mxfp8":
+                    sb = sc[r].view(np.uint8)  # H/32 E8M0 bytes, 4 per int32 word
+                    for b in range(H // 32):
+                        q, byte = orc.quant_group(x[t, b * 32:(b + 1) * 32], quant)
+                        assert np.array_equal(out[r, b * 32:(b + 1) * 32], q)
+                        assert (int(sc[r, b // 4]) >> (8 * (b % 4))) & 0xFF == byte == sb[b]
                     continue
                 for g in range(G):
                     q, s = orc.quant_group(x[t, g * 128:(g + 1) * 128], quant)
@@ -368,7 +398,7 @@ def pin_masked_repack(orc, rng):
     T, K, E, H = 20, 3, 5, 384
     idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
     x = torch_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
-    for quant in ("none", "fp8_f32", "fp8_ue8m0"):
+    for quant in ("none", "fp8_f32", "fp8_ue8m0", "mxfp8"):
         for cap in (T, 7):
             Lc = orc.layout(idx, E, "contig", align=16)
             Lm = orc.layout(idx, E, "masked", cap=cap)
@@ -386,19 +416,23 @@ def pin_masked_repack(orc, rng):
 
 
 def pin_fp8_roundtrip(orc, rng):
-    """combine(dequant(dispatch_fp8(x))) with identity experts ~ sum_k w_k x (2^-4 rel)."""
+    """combine(dequant(dispatch_fp8(x))) with identity experts ~ sum_k w_k x (2^-4 rel;
+    2^-3 for MXFP8, whose scale rule saturates the top of the block's binade)."""
     T, K, E, H = 12, 3, 4, 256
     idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
     w = rng.dirichlet(np.ones(K), size=T).astype(np.float32)
     x = torch_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
     xf = bf16_bits_to_f32(x).astype(np.float64)
     L = orc.layout(idx, E, "contig", align=4)
-    for quant in ("fp8_f32", "fp8_ue8m0"):
+    for quant in ("fp8_f32", "fp8_ue8m0", "mxfp8"):
         q, sc, _ = orc.dispatch(x, L["dst_row"], L["rows"], quant)
         dec = np.array([orc.e4m3_decode(c) for c in range(256)])[q]
         G = H // 128
         if quant == "fp8_f32":
             s = np.repeat(sc.astype(np.float64), 128, axis=1)
+        elif quant == "mxfp8":
+            eb = sc.view(np.uint8).reshape(sc.shape[0], -1).astype(np.float64)
+            s = np.repeat(np.exp2(eb - 127), 32, axis=1)
         else:
             eb = sc.view(np.uint8).reshape(sc.shape[0], -1)[:, :G].astype(np.float64)
             s = np.repeat(np.exp2(eb - 127), 128, axis=1)
@@ -406,9 +440,12 @@ def pin_fp8_roundtrip(orc, rng):
         out = bf16_bits_to_f32(orc.combine(y, w, L["dst_row"], H)).astype(np.float64)
         exact = w.astype(np.float64).sum(axis=1)[:, None] * xf
         amax = np.abs(xf).max()
-        assert (np.abs(out - exact) <= 2.0 ** -4 * np.abs(exact) + 2.0 ** -6 * amax).all()
+        # E4M3 rounding is within 2^-4 relative; the MX rule's scale puts the
+        # block maximum in [256, 512) and clamps above 448: up to 2^-3 there
+        rel = 2.0 ** -3 if quant == "mxfp8" else 2.0 ** -4
+        assert (np.abs(out - exact) <= rel * np.abs(exact) + 2.0 ** -6 * amax).all()
 
 
 ALL_PINS = [pin_bf16, pin_e4m3_decode, pin_e4m3_roundtrip_and_ties, pin_e4m3_nearest,
-            pin_quant_f32, pin_quant_ue8m0, pin_layout_bruteforce, pin_layout_bad_ids,
+            pin_quant_f32, pin_quant_ue8m0, pin_quant_mx, pin_layout_bruteforce, pin_layout_bad_ids,
             pin_dispatch, pin_combine, pin_masked_repack, pin_fp8_roundtrip]

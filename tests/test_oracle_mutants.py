@@ -24,6 +24,10 @@ MUTANTS = {
                         "fmaxf(group_amax(x, n), 1e-4f) / 240.0f;\n    for (int i = 0; i < n; ++i) q[i] = orc_e4m3_encode(orc_bf16_to_float(x[i]) / s);"),
     "amax_signed": ("float v = fabsf(orc_bf16_to_float(x[i]));", "float v = orc_bf16_to_float(x[i]);"),
     "ue8m0_floor": ("+ ((bits & 0x007FFFFFu) != 0u)", "+ 0"),
+    "mx_ceil_scale": ("e = ex - 1 + 127;", "e = ex + 127;"),
+    "mx_emax7": ("int byte = e - 8 > 0 ? e - 8 : 0;", "int byte = e - 7 > 0 ? e - 7 : 0;"),
+    "mx_scale_byte_layout": ("memcpy((uint8_t *)out_scales + (size_t)dst * (H / 32), mx, (size_t)(H / 32));",
+                             "memcpy((uint8_t *)out_scales + (size_t)dst * (H / 32), mx + (H > 32), (size_t)(H / 32 - (H > 32)));"),
     "layout_no_padding": ("offset[e] + round_up(count[e], align)", "offset[e] + count[e]"),
     "layout_k_descending": ("for (int k = 0; k < K; ++k) {\n            int i = t * K + k;",
                             "for (int k = K - 1; k >= 0; --k) {\n            int i = t * K + k;"),
