@@ -44,7 +44,8 @@ def algorithmic_bytes(w: workloads.Workload) -> dict:
     """Bytes the method must move per launch (padding and empty slots excluded)."""
     T, H, K = w.T, w.H, w.K
     G = H // 128
-    row = {"none": 2 * H, "fp8_f32": H + 4 * G, "fp8_ue8m0": H + 4 * ((G + 3) // 4)}[w.quant]
+    row = {"none": 2 * H, "fp8_f32": H + 4 * G, "fp8_ue8m0": H + 4 * ((G + 3) // 4),
+           "mxfp8": H + H // 32}[w.quant]
     return dict(
         layout=T * (4 * K + 4 * K + 4 * K),               # idx read, dst_row + row_src written
         dispatch=T * (2 * H + 4 * K + K * row),           # x read, dst_row read, K rows written
@@ -376,6 +377,7 @@ def run_ours(args, w):
     if e2e:
         line["e2e"] = e2e
     if not args.skip_decode:
+        line["dispatch_variants"] = measure_dispatch_variants(ep, w, L, x_d, dev)
         line["decode"] = measure_decode(ep, dev)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, idx, wts, x)
@@ -477,6 +479,35 @@ def measure_decode(ep, dev, reps=50):
         }
         del y, out_rows, slab, rows_c
         torch.cuda.empty_cache()
+    return res
+
+
+def measure_dispatch_variants(ep, w, L, x_d, dev, reps=20):
+    """ep_dispatch alone in every quantisation mode on the bench workload's layout
+    (inputs larger than L2); algorithmic bytes as in algorithmic_bytes()."""
+    import torch
+    res = {}
+    rows = L.rows_capacity
+    for quant in ("fp8_f32", "fp8_ue8m0", "mxfp8", "none"):
+        out_rows = torch.empty((rows, w.H), device=dev,
+                               dtype=torch.bfloat16 if quant == "none" else torch.uint8)
+        sc = None
+        if quant != "none":
+            sc = torch.empty((rows, ep.ep_scale_cols(w.H, quant)), device=dev,
+                             dtype=torch.float32 if quant == "fp8_f32" else torch.int32)
+        for _ in range(3):
+            ep.ep_dispatch(L, x_d, quant, out_rows=out_rows, out_scales=sc)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            ep.ep_dispatch(L, x_d, quant, out_rows=out_rows, out_scales=sc)
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        nbytes = algorithmic_bytes(w.with_(quant=quant))["dispatch"]
+        res[quant] = {"us": round(us, 2), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                      "tokens_per_s": round(w.T / (us * 1e-6), 1)}
+        del out_rows, sc
     return res
 
 

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libep.so")
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CAPACITY, EP_ERR_BAD_EXPERT_ID, EP_ERR_CUDA, EP_ERR_UNSUPPORTED = range(6)
 LAYOUT_KIND = {"contig": 0, "masked": 1}
-QUANT = {"none": 0, "fp8_f32": 1, "fp8_ue8m0": 2}
+QUANT = {"none": 0, "fp8_f32": 1, "fp8_ue8m0": 2, "mxfp8": 3}
 MAX_TOPK, MAX_EXPERTS, MAX_ALIGN = 32, 1024, 128
 
 
@@ -233,7 +233,8 @@ def ep_dispatch(layout: Layout, x: torch.Tensor, quant: str = "none",
     """Scatter (and quantise) x (bf16 [T, H]) into the layout's rows.
 
     Returns (out_rows, out_scales, row_w).  out_rows is bf16 [rows, H] or uint8
-    E4M3 bytes; out_scales fp32 [rows, H/128] or int32 [rows, ceil(H/512)].
+    E4M3 bytes; out_scales fp32 [rows, H/128] (fp8_f32), int32 [rows, ceil(H/512)]
+    (fp8_ue8m0) or int32 [rows, H/128] holding H/32 E8M0 bytes (mxfp8).
     """
     T, H = x.shape
     if x.dtype != torch.bfloat16:

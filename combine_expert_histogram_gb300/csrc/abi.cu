@@ -68,7 +68,7 @@ ep_status_t check_layout(const ep_layout_t *L) {
 ep_status_t check_hidden(int32_t H, ep_quant_t quant) {
     if (H <= 0) return EP_ERR_INVALID_ARG;
     if (quant == EP_QUANT_NONE) return H % 8 == 0 ? EP_OK : EP_ERR_INVALID_ARG;
-    if (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_FP8_UE8M0)
+    if (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_FP8_UE8M0 || quant == EP_QUANT_MXFP8)
         return H % 128 == 0 ? EP_OK : EP_ERR_INVALID_ARG;
     return EP_ERR_INVALID_ARG;
 }
@@ -101,7 +101,7 @@ int64_t ep_rows_capacity(const ep_layout_t *L) {
 
 int64_t ep_scale_cols(int32_t hidden, ep_quant_t quant) {
     if (check_hidden(hidden, quant) != EP_OK) return -1;
-    if (quant == EP_QUANT_FP8_F32) return hidden / 128;
+    if (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_MXFP8) return hidden / 128;
     if (quant == EP_QUANT_FP8_UE8M0) return (hidden / 128 + 3) / 4;
     return 0;
 }

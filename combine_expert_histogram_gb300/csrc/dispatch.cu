@@ -1,10 +1,13 @@
 // ep_dispatch kernels: scatter token rows into the layout, fused with dynamic
-// 1x128 FP8-E4M3 quantisation (fp32 or packed UE8M0 scales).
+// 1x128 FP8-E4M3 quantisation (fp32 or packed UE8M0 scales) or 1x32 MXFP8.
 //
 // Format and scale conventions follow SGLang PR "[Feature] Add DeepEPv2
 // (ElasticBuffer) MoE A2A backend" ("Supported scope": dynamic blockwise FP8;
 // "Implementation": Hopper FP32 scales and Blackwell packed UE8M0 scales) and
-// the vLLM tools/ep_kernels deepep_v2 commit ("FP8 block-quantized dispatch").
+// the vLLM tools/ep_kernels deepep_v2 commit ("FP8 block-quantized dispatch");
+// MXFP8 is the "1x32 MXFP8 ... with dynamic activation scaling" format of the
+// SGLang discussion "deepep v2 support?", scaled by the OCP Microscaling (MX)
+// v1.0 rule X = 2^(floor(log2 amax) - 8).
 //
 // HBM-bound: each token row is read once and written K times (80 % of the
 // bytes are writes).  One CTA owns one token:
@@ -73,7 +76,8 @@ __global__ void __launch_bounds__(kMaxThreads)
     // staged bytes: the row (H fp8 or 2H bf16), then the scale row
     const int row_bytes = Q == EP_QUANT_NONE ? 2 * H : H;
     const int P4 = ((G + 3) >> 2) * 4;  // UE8M0 scale bytes per row
-    const int scale_bytes = Q == EP_QUANT_FP8_F32 ? 4 * G : Q == EP_QUANT_FP8_UE8M0 ? P4 : 0;
+    const int scale_bytes = (Q == EP_QUANT_FP8_F32 || Q == EP_QUANT_MXFP8) ? 4 * G
+                            : Q == EP_QUANT_FP8_UE8M0 ? P4 : 0;
     uint8_t *srow = stage;
     uint8_t *sscale = stage + row_bytes;
     __shared__ int32_t sdst[EP_MAX_TOPK];
@@ -113,6 +117,21 @@ __global__ void __launch_bounds__(kMaxThreads)
                 q.z = fp8x4(__fdiv_rn(v[8], s), __fdiv_rn(v[9], s), __fdiv_rn(v[10], s), __fdiv_rn(v[11], s));
                 q.w = fp8x4(__fdiv_rn(v[12], s), __fdiv_rn(v[13], s), __fdiv_rn(v[14], s), __fdiv_rn(v[15], s));
                 if (sub == 0) reinterpret_cast<float *>(sscale)[g] = s;
+            } else if (Q == EP_QUANT_MXFP8) {
+                // two lanes hold one 32-element block: X = 2^(floor(log2 amax) - 8),
+                // clamped at 2^-127; byte = log2(X) + 127; multiply by 1/X = 2^(127-byte)
+                float bmax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+                bmax = fmaxf(bmax, __shfl_xor_sync(gmask, bmax, 1));
+                const int be = (int)((__float_as_uint(bmax) >> 23) & 0xffu);  // 0: zero/subnormal
+                const int byte = be > 8 ? be - 8 : 0;
+                const float inv = __uint_as_float((uint32_t)(254 - byte) << 23);
+                q.x = fp8x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv), __fmul_rn(v[3], inv));
+                q.y = fp8x4(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv), __fmul_rn(v[6], inv), __fmul_rn(v[7], inv));
+                q.z = fp8x4(__fmul_rn(v[8], inv), __fmul_rn(v[9], inv), __fmul_rn(v[10], inv), __fmul_rn(v[11], inv));
+                q.w = fp8x4(__fmul_rn(v[12], inv), __fmul_rn(v[13], inv), __fmul_rn(v[14], inv), __fmul_rn(v[15], inv));
+                if ((sub & 1) == 0) sscale[g * 4 + (sub >> 1)] = (uint8_t)byte;
             } else {
                 // scale rounded up to a power of two 2^(e-127); multiply by 2^(127-e)
                 const uint32_t bits = __float_as_uint(s);
@@ -169,7 +188,8 @@ cudaError_t launch_q(const ep_layout_t &L, const void *x, int H, void *out_rows,
                      void *out_scales, const float *topk_w, float *row_w, cudaStream_t stream) {
     const int G = H / 128;
     const int row_bytes = Q == EP_QUANT_NONE ? 2 * H : H;
-    const int scale_bytes = Q == EP_QUANT_FP8_F32 ? 4 * G : Q == EP_QUANT_FP8_UE8M0 ? ((G + 3) / 4) * 4 : 0;
+    const int scale_bytes = (Q == EP_QUANT_FP8_F32 || Q == EP_QUANT_MXFP8) ? 4 * G
+                            : Q == EP_QUANT_FP8_UE8M0 ? ((G + 3) / 4) * 4 : 0;
     const size_t smem = (size_t)row_bytes + (size_t)scale_bytes;
     // one slot per 16 elements (FP8) or per 16-byte chunk (bf16), up to 512 threads
     int slots = Q == EP_QUANT_NONE ? H / 8 : G * 8;
@@ -181,7 +201,8 @@ cudaError_t launch_q(const ep_layout_t &L, const void *x, int H, void *out_rows,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
     }
-    const bool bulk_scales = Q == EP_QUANT_FP8_F32 && (scale_bytes % 16) == 0 &&
+    const bool bulk_scales = (Q == EP_QUANT_FP8_F32 || Q == EP_QUANT_MXFP8) &&
+                             (scale_bytes % 16) == 0 &&
                              (reinterpret_cast<uintptr_t>(out_scales) % 16) == 0;
     // programmatic dependent of the layout: x is loaded and quantised while
     // the layout kernels finish
@@ -202,6 +223,8 @@ cudaError_t launch_dispatch(const ep_layout_t &L, const void *x, int H, ep_quant
             return launch_q<EP_QUANT_NONE>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
         case EP_QUANT_FP8_F32:
             return launch_q<EP_QUANT_FP8_F32>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+        case EP_QUANT_MXFP8:
+            return launch_q<EP_QUANT_MXFP8>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
         default:
             return launch_q<EP_QUANT_FP8_UE8M0>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
     }

@@ -65,7 +65,7 @@ cudaError_t launch_masked_repack(const ep_layout_t &L, const void *rows,
     const int E = L.num_experts;
     const int row_bytes = quant == EP_QUANT_NONE ? 2 * H : H;
     const int G = H / 128;
-    const int scale_bytes = quant == EP_QUANT_FP8_F32 ? 4 * G
+    const int scale_bytes = (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_MXFP8) ? 4 * G
                             : quant == EP_QUANT_FP8_UE8M0 ? 4 * ((G + 3) / 4) : 0;
     // Enough warps to keep HBM busy: the valid rows number at most T*K.
     const long long rows_max = (long long)L.num_tokens * L.num_topk;

@@ -78,8 +78,11 @@ typedef enum ep_layout_kind {
 typedef enum ep_quant {
     EP_QUANT_NONE = 0,     /* bf16 rows                                           */
     EP_QUANT_FP8_F32 = 1,  /* E4M3 rows + fp32 scale per 1x128 group  [rows, H/128]  */
-    EP_QUANT_FP8_UE8M0 = 2 /* E4M3 rows + UE8M0 exponent per group, 4 per int32 word
+    EP_QUANT_FP8_UE8M0 = 2, /* E4M3 rows + UE8M0 exponent per group, 4 per int32 word
                               [rows, ceil(H/512)]                                   */
+    EP_QUANT_MXFP8 = 3      /* E4M3 rows + E8M0 scale per 1x32 block, 4 per int32 word
+                              [rows, H/128] ([DISC-26563]: 1x32 MXFP8 with dynamic
+                              activation scaling; OCP MX v1.0 conversion rule)       */
 } ep_quant_t;
 
 #define EP_MAX_TOPK 32     /* [PR-24443] review: kNumTopk <= 32 */
@@ -128,8 +131,8 @@ const char *ep_status_str(ep_status_t status);
  * (the worst case of the padded scan), masked E*capacity.  -1 on a bad layout. */
 int64_t ep_rows_capacity(const ep_layout_t *layout);
 
-/* 32-bit scale words per row: H/128 (fp32 scales), ceil(H/512) (packed UE8M0),
- * 0 (bf16); -1 if `hidden` is not valid for `quant`. */
+/* 32-bit scale words per row: H/128 (fp32 scales, or MXFP8's H/32 E8M0 bytes),
+ * ceil(H/512) (packed UE8M0), 0 (bf16); -1 if `hidden` is not valid for `quant`. */
 int64_t ep_scale_cols(int32_t hidden, ep_quant_t quant);
 
 /* Bytes of device scratch ep_layout() needs for this shape (may be 0).  The
@@ -182,6 +185,10 @@ ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *layout, void *
  *   FP8_UE8M0: s rounded up to 2^(e-127) (e = biased exponent of s, plus one
  *              when s is not a power of two); q = E4M3_rn_satfinite(x * 2^(127-e));
  *              byte g%4 of int32 word g/4 (little-endian) = e; unused bytes 127.
+ *   MXFP8:     per 32-element block b: X = 2^(floor(log2 amax) - 8) (8 = exponent
+ *              of E4M3's largest normal), clamped at 2^-127 (all-zero and
+ *              subnormal blocks); q = E4M3_rn_satfinite(x / X) (values between
+ *              448 and 512 saturate); byte b%4 of int32 word b/4 = log2(X) + 127.
  * and the same bytes are written to every row dst_row[t*K+k] >= 0.
  */
 ep_status_t ep_dispatch(const ep_layout_t *layout, const void *x, int32_t hidden,

@@ -92,6 +92,8 @@ class Oracle:
         L.orc_dispatch.argtypes = [P, I, I, I, I, P, P, P, P, P]
         L.orc_combine.restype = None
         L.orc_combine.argtypes = [P, P, P, I, I, I, P]
+        L.orc_scales_mn_major.restype = None
+        L.orc_scales_mn_major.argtypes = [P, I, I, I, I, I, P]
         L.orc_masked_repack.restype = I
         L.orc_masked_repack.argtypes = [P, P, I, I, P, P, I, I, P, P, P]
         self.lib = L
@@ -188,6 +190,21 @@ class Oracle:
         self.lib.orc_combine(_p(y), _p(w), _p(d), T, K, H, _p(out))
         return out
 
+    # ------------------------------------------------- MN-major scale layout
+    def scales_mn_major(self, row_major: np.ndarray, layout: str, E: int = 0, cap: int = 0,
+                        fill: int = 0) -> np.ndarray:
+        """Row-major packed UE8M0 words [rows, P] -> the MN-major buffer (1-D int32)."""
+        rm = np.ascontiguousarray(row_major, dtype=np.int32)
+        rows, P = rm.shape
+        if layout == "masked":
+            n = E * P * ((cap + 3) // 4 * 4)
+        else:
+            n = P * ((rows + 3) // 4 * 4)
+        out = np.full(max(n, 1), fill, dtype=np.int32)[:n]
+        self.lib.orc_scales_mn_major(_p(rm), rows, P, 1 if layout == "masked" else 0, E, cap,
+                                     _p(out))
+        return out
+
     # --------------------------------------------------------- masked repack
     def masked_repack(self, rows_buf: np.ndarray, scales, H: int, quant: str,
                       offset: np.ndarray, count: np.ndarray, E: int, cap: int, fill: int = 0):
@@ -222,6 +239,6 @@ def __getattr__(name):
     # module-level convenience: oracle.layout(...) == oracle.default().layout(...)
     if name in ("bf16_round", "bf16_round_array", "bf16_to_float", "e4m3_encode",
                 "e4m3_encode_array", "e4m3_decode", "quant_group", "layout", "dispatch",
-                "combine", "masked_repack"):
+                "combine", "masked_repack", "scales_mn_major"):
         return getattr(default(), name)
     raise AttributeError(name)

@@ -275,6 +275,31 @@ void orc_combine(const uint16_t *y, const float *topk_w, const int32_t *dst_row,
     }
 }
 
+/* ------------------------------------------------- MN-major scale layout */
+
+/* Packed UE8M0 scale words re-laid "MN-major" for a grouped GEMM that loads
+ * per-row scale factors with TMA: word p of every row is contiguous along the
+ * rows, each column padded to a multiple of 4 rows (16 bytes).
+ *   contiguous layout (rows = the row space's capacity):
+ *       out[p * roundup(rows, 4) + r]                 = row_major[r * P + p]
+ *   masked layout (row r = e * cap + s):
+ *       out[(e * P + p) * roundup(cap, 4) + s]        = row_major[r * P + p]
+ * Entries of the padding are not written. */
+void orc_scales_mn_major(const int32_t *row_major, int rows, int P, int masked, int E,
+                         int cap, int32_t *out) {
+    if (masked) {
+        int cap4 = (cap + 3) / 4 * 4;
+        for (int e = 0; e < E; ++e)
+            for (int s = 0; s < cap; ++s)
+                for (int p = 0; p < P; ++p)
+                    out[((size_t)e * P + p) * cap4 + s] = row_major[((size_t)e * cap + s) * P + p];
+    } else {
+        int rows4 = (rows + 3) / 4 * 4;
+        for (int r = 0; r < rows; ++r)
+            for (int p = 0; p < P; ++p) out[(size_t)p * rows4 + r] = row_major[(size_t)r * P + p];
+    }
+}
+
 /* --------------------------------------------------------- masked repack */
 
 /* slab[e, s, :] = rows[offset[e] + s, :] for s < min(count[e], cap), and the

@@ -67,6 +67,9 @@ void orc_dispatch(const uint16_t *x, int T, int K, int H, int quant,
 void orc_combine(const uint16_t *y, const float *topk_w, const int32_t *dst_row,
                  int T, int K, int H, uint16_t *out);
 
+void orc_scales_mn_major(const int32_t *row_major, int rows, int P, int masked, int E,
+                         int cap, int32_t *out);
+
 int orc_masked_repack(const void *rows, const void *row_scales, int H, int quant,
                       const int32_t *offset, const int32_t *count, int E, int cap,
                       void *slab, void *slab_scales, int32_t *masked_m);

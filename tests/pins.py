@@ -446,6 +446,27 @@ def pin_fp8_roundtrip(orc, rng):
         assert (np.abs(out - exact) <= rel * np.abs(exact) + 2.0 ** -6 * amax).all()
 
 
+def pin_scales_mn_major(orc, rng):
+    """MN-major re-layout == numpy's transpose of the row-major words; every
+    scale column starts on a 16-byte boundary."""
+    for rows, P in ((13, 3), (16, 14), (1, 1), (130, 2)):
+        rm = rng.integers(-2**31, 2**31 - 1, size=(rows, P), dtype=np.int64).astype(np.int32)
+        out = orc.scales_mn_major(rm, "contig", fill=-7)
+        rows4 = (rows + 3) // 4 * 4
+        assert out.size == P * rows4 and (rows4 * 4) % 16 == 0
+        grid = out.reshape(P, rows4)
+        assert np.array_equal(grid[:, :rows].T, rm)
+        assert (grid[:, rows:] == -7).all()
+    for E, cap, P in ((3, 5, 2), (4, 8, 14), (2, 1, 1)):
+        rm = rng.integers(-2**31, 2**31 - 1, size=(E * cap, P), dtype=np.int64).astype(np.int32)
+        out = orc.scales_mn_major(rm, "masked", E=E, cap=cap, fill=-7)
+        cap4 = (cap + 3) // 4 * 4
+        grid = out.reshape(E, P, cap4)
+        assert np.array_equal(grid[:, :, :cap].transpose(0, 2, 1).reshape(E * cap, P), rm)
+        assert (grid[:, :, cap:] == -7).all()
+
+
 ALL_PINS = [pin_bf16, pin_e4m3_decode, pin_e4m3_roundtrip_and_ties, pin_e4m3_nearest,
             pin_quant_f32, pin_quant_ue8m0, pin_quant_mx, pin_layout_bruteforce, pin_layout_bad_ids,
-            pin_dispatch, pin_combine, pin_masked_repack, pin_fp8_roundtrip]
+            pin_dispatch, pin_combine, pin_masked_repack, pin_fp8_roundtrip,
+            pin_scales_mn_major]

@@ -54,6 +54,11 @@ MID = [
                        layout="masked", quant="fp8_ue8m0", cap=16, R=16, seed=8),
     workloads.Workload("h128", T=5000, H=128, E=32, K=2, routing="softmax",
                        layout="contig", quant="fp8_f32", align=32, seed=9),
+    # MXFP8: scale rows of 20 bytes (plain stores) and of 224 bytes (bulk stores)
+    workloads.Workload("mxfp8_ragged", T=3001, H=640, E=64, K=8, routing="softmax",
+                       layout="contig", quant="mxfp8", align=128, seed=12),
+    workloads.Workload("mxfp8_dsv3", T=2000, H=7168, E=256, K=8, routing="grouped_sigmoid",
+                       layout="masked", quant="mxfp8", cap=2000, seed=13),
     # > 128 tiles of 2048 entries: tiles of several passes
     workloads.Workload("multipass", T=40000, H=128, E=64, K=8, routing="softmax",
                        layout="contig", quant="fp8_ue8m0", align=128, R=4, seed=10),
@@ -137,7 +142,7 @@ def test_special_values_quantise_like_oracle():
     x = workloads.bf16_bits_from_f32(xf)
     idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
     wts = rng.random((T, K)).astype(np.float32)
-    for quant in ("fp8_f32", "fp8_ue8m0"):
+    for quant in ("fp8_f32", "fp8_ue8m0", "mxfp8"):
         w = workloads.Workload("sv", T=T, H=H, E=E, K=K, routing="softmax", layout="contig",
                                quant=quant, align=16)
         case = dict(idx=idx, w=wts, x=x, idx_d=torch.from_numpy(idx).cuda(),
@@ -148,7 +153,7 @@ def test_special_values_quantise_like_oracle():
         gh.check_dispatch(w, case, g, ref)
 
 
-@pytest.mark.parametrize("quant", ["none", "fp8_f32", "fp8_ue8m0"])
+@pytest.mark.parametrize("quant", ["none", "fp8_f32", "fp8_ue8m0", "mxfp8"])
 def test_masked_repack_matches_masked_dispatch(quant):
     from combine_expert_histogram_gb300 import binding as ep
     w = workloads.CONFIGS["qwen3_30b_a3b_decode"].with_(quant=quant)
