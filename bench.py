@@ -488,13 +488,10 @@ def measure_dispatch_variants(ep, w, L, x_d, dev, reps=20):
     import torch
     res = {}
     rows = L.rows_capacity
-    for quant in ("fp8_f32", "fp8_ue8m0", "mxfp8", "none"):
+    for quant in ("fp8_f32", "fp8_ue8m0", "fp8_ue8m0_mn", "mxfp8", "none"):
         out_rows = torch.empty((rows, w.H), device=dev,
                                dtype=torch.bfloat16 if quant == "none" else torch.uint8)
-        sc = None
-        if quant != "none":
-            sc = torch.empty((rows, ep.ep_scale_cols(w.H, quant)), device=dev,
-                             dtype=torch.float32 if quant == "fp8_f32" else torch.int32)
+        sc = ep.scale_buffer(L, w.H, quant, device=dev)
         for _ in range(3):
             ep.ep_dispatch(L, x_d, quant, out_rows=out_rows, out_scales=sc)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -504,7 +501,7 @@ def measure_dispatch_variants(ep, w, L, x_d, dev, reps=20):
         b.record()
         torch.cuda.synchronize()
         us = a.elapsed_time(b) * 1e3 / reps
-        nbytes = algorithmic_bytes(w.with_(quant=quant))["dispatch"]
+        nbytes = algorithmic_bytes(w.with_(quant=quant.replace("_mn", "")))["dispatch"]
         res[quant] = {"us": round(us, 2), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                       "tokens_per_s": round(w.T / (us * 1e-6), 1)}
         del out_rows, sc

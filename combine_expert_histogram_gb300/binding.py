@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libep.so")
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CAPACITY, EP_ERR_BAD_EXPERT_ID, EP_ERR_CUDA, EP_ERR_UNSUPPORTED = range(6)
 LAYOUT_KIND = {"contig": 0, "masked": 1}
-QUANT = {"none": 0, "fp8_f32": 1, "fp8_ue8m0": 2, "mxfp8": 3}
+QUANT = {"none": 0, "fp8_f32": 1, "fp8_ue8m0": 2, "mxfp8": 3, "fp8_ue8m0_mn": 4}
 MAX_TOPK, MAX_EXPERTS, MAX_ALIGN = 32, 1024, 128
 
 
@@ -51,7 +51,8 @@ class _Layout(ctypes.Structure):
 
 _lib = None
 
-EXPORTS = ("ep_status_str", "ep_rows_capacity", "ep_scale_cols", "ep_layout_workspace_bytes",
+EXPORTS = ("ep_status_str", "ep_rows_capacity", "ep_scale_cols", "ep_scale_words",
+           "ep_layout_workspace_bytes",
            "ep_layout", "ep_dispatch", "ep_combine", "ep_masked_repack", "ep_layout_noalloc")
 NOALLOC_SCRATCH_BYTES = 256 * 1024
 
@@ -73,6 +74,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ep_rows_capacity.argtypes = [LP]
     L.ep_scale_cols.restype = I64
     L.ep_scale_cols.argtypes = [I32, ctypes.c_int]
+    L.ep_scale_words.restype = I64
+    L.ep_scale_words.argtypes = [LP, I32, ctypes.c_int]
     L.ep_layout_workspace_bytes.restype = SZ
     L.ep_layout_workspace_bytes.argtypes = [LP]
     L.ep_layout.restype = ctypes.c_int
@@ -198,6 +201,35 @@ def ep_scale_cols(hidden: int, quant: str) -> int:
     return int(load_library().ep_scale_cols(hidden, QUANT[quant]))
 
 
+def _shape_struct(layout: Layout) -> _Layout:
+    c = _Layout()
+    c.num_tokens, c.num_topk, c.num_experts = layout.num_tokens, layout.num_topk, layout.num_experts
+    c.num_ranks, c.kind, c.align = layout.num_ranks, LAYOUT_KIND[layout.kind], layout.align
+    c.capacity, c.max_tokens = layout.capacity, layout.max_tokens
+    return c
+
+
+def ep_scale_words(layout: Layout, hidden: int, quant: str) -> int:
+    return int(load_library().ep_scale_words(ctypes.byref(_shape_struct(layout)), hidden,
+                                             QUANT[quant]))
+
+
+def scale_buffer(layout: Layout, hidden: int, quant: str, device=None) -> Optional[torch.Tensor]:
+    """An uninitialised scale buffer shaped for ``quant`` on this layout."""
+    if quant == "none":
+        return None
+    dev = device if device is not None else layout.dst_row.device
+    cols = ep_scale_cols(hidden, quant)
+    if quant == "fp8_ue8m0_mn":
+        if layout.kind == "masked":
+            shape = (layout.num_experts, cols, (layout.capacity + 3) // 4 * 4)
+        else:
+            shape = (cols, (max(layout.rows_capacity, 1) + 3) // 4 * 4)
+        return torch.empty(shape, device=dev, dtype=torch.int32)
+    return torch.empty((max(layout.rows_capacity, 1), cols), device=dev,
+                       dtype=torch.float32 if quant == "fp8_f32" else torch.int32)
+
+
 def ep_layout_workspace_bytes(layout: Layout) -> int:
     c = _Layout()
     c.num_tokens, c.num_topk, c.num_experts = layout.num_tokens, layout.num_topk, layout.num_experts
@@ -245,9 +277,7 @@ def ep_dispatch(layout: Layout, x: torch.Tensor, quant: str = "none",
         out_rows = torch.empty((max(rows, 1), H), device=dev,
                                dtype=torch.bfloat16 if quant == "none" else torch.uint8)
     if quant != "none" and out_scales is None:
-        cols = ep_scale_cols(H, quant)
-        out_scales = torch.empty((max(rows, 1), cols), device=dev,
-                                 dtype=torch.float32 if quant == "fp8_f32" else torch.int32)
+        out_scales = scale_buffer(layout, H, quant, device=dev)
     if topk_w is not None and row_w is None:
         row_w = torch.empty(max(rows, 1), device=dev, dtype=torch.float32)
     code = load_library().ep_dispatch(ctypes.byref(layout.struct()), _ptr(x), H, QUANT[quant],
@@ -282,8 +312,12 @@ def ep_masked_repack(layout: Layout, rows: torch.Tensor, row_scales: Optional[to
     if slab is None:
         slab = torch.empty((E, capacity, H), device=dev, dtype=rows.dtype)
     if row_scales is not None and slab_scales is None:
-        slab_scales = torch.empty((E, capacity, row_scales.shape[-1]), device=dev,
-                                  dtype=row_scales.dtype)
+        if quant == "fp8_ue8m0_mn":
+            slab_scales = torch.empty((E, ep_scale_cols(H, quant), (capacity + 3) // 4 * 4),
+                                      device=dev, dtype=row_scales.dtype)
+        else:
+            slab_scales = torch.empty((E, capacity, row_scales.shape[-1]), device=dev,
+                                      dtype=row_scales.dtype)
     if masked_m is None:
         masked_m = torch.empty(E, device=dev, dtype=torch.int32)
     code = load_library().ep_masked_repack(ctypes.byref(layout.struct()), _ptr(rows),

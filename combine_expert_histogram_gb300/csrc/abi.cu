@@ -68,7 +68,8 @@ ep_status_t check_layout(const ep_layout_t *L) {
 ep_status_t check_hidden(int32_t H, ep_quant_t quant) {
     if (H <= 0) return EP_ERR_INVALID_ARG;
     if (quant == EP_QUANT_NONE) return H % 8 == 0 ? EP_OK : EP_ERR_INVALID_ARG;
-    if (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_FP8_UE8M0 || quant == EP_QUANT_MXFP8)
+    if (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_FP8_UE8M0 || quant == EP_QUANT_MXFP8 ||
+        quant == EP_QUANT_FP8_UE8M0_MN)
         return H % 128 == 0 ? EP_OK : EP_ERR_INVALID_ARG;
     return EP_ERR_INVALID_ARG;
 }
@@ -102,8 +103,17 @@ int64_t ep_rows_capacity(const ep_layout_t *L) {
 int64_t ep_scale_cols(int32_t hidden, ep_quant_t quant) {
     if (check_hidden(hidden, quant) != EP_OK) return -1;
     if (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_MXFP8) return hidden / 128;
-    if (quant == EP_QUANT_FP8_UE8M0) return (hidden / 128 + 3) / 4;
+    if (quant == EP_QUANT_FP8_UE8M0 || quant == EP_QUANT_FP8_UE8M0_MN) return (hidden / 128 + 3) / 4;
     return 0;
+}
+
+int64_t ep_scale_words(const ep_layout_t *L, int32_t hidden, ep_quant_t quant) {
+    if (check_shape(L) != EP_OK || check_hidden(hidden, quant) != EP_OK) return -1;
+    const int64_t cols = ep_scale_cols(hidden, quant);
+    if (quant != EP_QUANT_FP8_UE8M0_MN) return rows_capacity(*L) * cols;
+    if (L->kind == EP_LAYOUT_MASKED)
+        return (int64_t)L->num_experts * cols * ((L->capacity + 3) / 4 * 4);
+    return cols * ((rows_capacity(*L) + 3) / 4 * 4);
 }
 
 size_t ep_layout_workspace_bytes(const ep_layout_t *L) {

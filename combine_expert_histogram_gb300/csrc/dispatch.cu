@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kMaxThreads)
     dispatch_kernel(const uint16_t *__restrict__ x, int K, int H,
                     const int32_t *__restrict__ dst_row, uint8_t *__restrict__ out,
                     void *__restrict__ scales, const float *__restrict__ topk_w,
-                    float *__restrict__ row_w, bool bulk_scales) {
+                    float *__restrict__ row_w, bool bulk_scales, int mn_stride, int mn_cap) {
     // bulk_scales: fp32 scale rows are a multiple of 16 bytes and `scales` is
     // 16-byte aligned, so they go out with the TMA too
     extern __shared__ __align__(128) uint8_t stage[];
@@ -76,13 +76,14 @@ __global__ void __launch_bounds__(kMaxThreads)
     // staged bytes: the row (H fp8 or 2H bf16), then the scale row
     const int row_bytes = Q == EP_QUANT_NONE ? 2 * H : H;
     const int P4 = ((G + 3) >> 2) * 4;  // UE8M0 scale bytes per row
+    constexpr bool kUe8m0 = Q == EP_QUANT_FP8_UE8M0 || Q == EP_QUANT_FP8_UE8M0_MN;
     const int scale_bytes = (Q == EP_QUANT_FP8_F32 || Q == EP_QUANT_MXFP8) ? 4 * G
-                            : Q == EP_QUANT_FP8_UE8M0 ? P4 : 0;
+                            : kUe8m0 ? P4 : 0;
     uint8_t *srow = stage;
     uint8_t *sscale = stage + row_bytes;
     __shared__ int32_t sdst[EP_MAX_TOPK];
 
-    if (Q == EP_QUANT_FP8_UE8M0 && threadIdx.x < P4 - G) sscale[G + threadIdx.x] = 127;  // 2^0
+    if (kUe8m0 && threadIdx.x < P4 - G) sscale[G + threadIdx.x] = 127;  // 2^0
 
     const uint16_t *xr = x + (size_t)t * H;
     if (Q == EP_QUANT_NONE) {
@@ -165,15 +166,19 @@ __global__ void __launch_bounds__(kMaxThreads)
         }
         bulk_commit();
     }
-    // remaining scale rows: 4-byte words by the other threads
+    // remaining scale rows: 4-byte words by the other threads (row-major, or
+    // MN-major: word wd of row d at wd*stride + d, per expert for masked)
     if (Q != EP_QUANT_NONE && !bulk_scales) {
         const int words = scale_bytes >> 2;
         for (int j = threadIdx.x; j < K * words; j += blockDim.x) {
             const int k = j / words, wd = j - k * words;
             const int d = sdst[k];
-            if (d >= 0)
-                reinterpret_cast<uint32_t *>(scales)[(size_t)d * words + wd] =
-                    reinterpret_cast<const uint32_t *>(sscale)[wd];
+            if (d < 0) continue;
+            size_t at = (size_t)d * words + wd;
+            if (Q == EP_QUANT_FP8_UE8M0_MN)
+                at = mn_cap ? ((size_t)(d / mn_cap) * words + wd) * mn_stride + (size_t)(d % mn_cap)
+                            : (size_t)wd * mn_stride + d;
+            reinterpret_cast<uint32_t *>(scales)[at] = reinterpret_cast<const uint32_t *>(sscale)[wd];
         }
     }
     if (row_w && threadIdx.x < K) {
@@ -189,7 +194,8 @@ cudaError_t launch_q(const ep_layout_t &L, const void *x, int H, void *out_rows,
     const int G = H / 128;
     const int row_bytes = Q == EP_QUANT_NONE ? 2 * H : H;
     const int scale_bytes = (Q == EP_QUANT_FP8_F32 || Q == EP_QUANT_MXFP8) ? 4 * G
-                            : Q == EP_QUANT_FP8_UE8M0 ? ((G + 3) / 4) * 4 : 0;
+                            : (Q == EP_QUANT_FP8_UE8M0 || Q == EP_QUANT_FP8_UE8M0_MN) ? ((G + 3) / 4) * 4
+                            : 0;
     const size_t smem = (size_t)row_bytes + (size_t)scale_bytes;
     // one slot per 16 elements (FP8) or per 16-byte chunk (bf16), up to 512 threads
     int slots = Q == EP_QUANT_NONE ? H / 8 : G * 8;
@@ -206,10 +212,19 @@ cudaError_t launch_q(const ep_layout_t &L, const void *x, int H, void *out_rows,
                              (reinterpret_cast<uintptr_t>(out_scales) % 16) == 0;
     // programmatic dependent of the layout: x is loaded and quantised while
     // the layout kernels finish
+    // MN-major scale columns: padded row space (contiguous) or padded capacity per expert
+    const bool masked = L.kind == EP_LAYOUT_MASKED;
+    const long long rows_cap = masked ? (long long)L.num_experts * L.capacity
+                                      : (long long)L.num_tokens * L.num_topk +
+                                            (long long)(L.num_tokens * L.num_topk < L.num_experts
+                                                            ? L.num_tokens * L.num_topk
+                                                            : L.num_experts) * (L.align - 1);
+    const int mn_cap = masked ? L.capacity : 0;
+    const int mn_stride = masked ? (L.capacity + 3) / 4 * 4 : (int)((rows_cap + 3) / 4 * 4);
     return launch_kernel(dispatch_kernel<Q>, L.num_tokens, threads, smem, stream, true,
                          static_cast<const uint16_t *>(x), L.num_topk, H, L.dst_row,
                          static_cast<uint8_t *>(out_rows), out_scales, topk_w, row_w,
-                         bulk_scales);
+                         bulk_scales, mn_stride, mn_cap);
 }
 
 }  // namespace
@@ -225,6 +240,8 @@ cudaError_t launch_dispatch(const ep_layout_t &L, const void *x, int H, ep_quant
             return launch_q<EP_QUANT_FP8_F32>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
         case EP_QUANT_MXFP8:
             return launch_q<EP_QUANT_MXFP8>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+        case EP_QUANT_FP8_UE8M0_MN:
+            return launch_q<EP_QUANT_FP8_UE8M0_MN>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
         default:
             return launch_q<EP_QUANT_FP8_UE8M0>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
     }

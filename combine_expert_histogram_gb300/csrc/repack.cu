@@ -19,7 +19,10 @@ __global__ void __launch_bounds__(kThreads)
                   int row_bytes, int scale_bytes, const int32_t *__restrict__ offset,
                   const int32_t *__restrict__ count, int E, int cap,
                   uint8_t *__restrict__ slab, uint8_t *__restrict__ slab_scales,
-                  int32_t *__restrict__ masked_m, int32_t *__restrict__ status) {
+                  int32_t *__restrict__ masked_m, int32_t *__restrict__ status,
+                  int mn_src_stride, int mn_dst_stride) {
+    // mn_src_stride > 0: scale words are MN-major (source column stride over the
+    // contiguous row space; destination [E][words][mn_dst_stride])
     extern __shared__ int32_t pre[];  // [E+1]
     __shared__ int32_t scan_tmp[kThreads / 32];
     block_exclusive_scan<kThreads>(
@@ -48,7 +51,13 @@ __global__ void __launch_bounds__(kThreads)
         const uint8_t *sp = rows + src * row_bytes;
         uint8_t *dp = slab + dst * row_bytes;
         for (int b = lane * 16; b < row_bytes; b += 32 * 16) st_v4(dp + b, ld_stream(sp + b));
-        if (scale_bytes) {
+        if (scale_bytes && mn_src_stride) {
+            const uint32_t *ss = reinterpret_cast<const uint32_t *>(row_scales);
+            uint32_t *ds = reinterpret_cast<uint32_t *>(slab_scales);
+            const int words = scale_bytes / 4;
+            for (int b = lane; b < words; b += 32)
+                ds[((size_t)lo * words + b) * mn_dst_stride + s] = __ldg(ss + (size_t)b * mn_src_stride + src);
+        } else if (scale_bytes) {
             const uint32_t *ss = reinterpret_cast<const uint32_t *>(row_scales + src * scale_bytes);
             uint32_t *ds = reinterpret_cast<uint32_t *>(slab_scales + dst * scale_bytes);
             for (int b = lane; b < scale_bytes / 4; b += 32) ds[b] = __ldg(ss + b);
@@ -66,7 +75,15 @@ cudaError_t launch_masked_repack(const ep_layout_t &L, const void *rows,
     const int row_bytes = quant == EP_QUANT_NONE ? 2 * H : H;
     const int G = H / 128;
     const int scale_bytes = (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_MXFP8) ? 4 * G
-                            : quant == EP_QUANT_FP8_UE8M0 ? 4 * ((G + 3) / 4) : 0;
+                            : (quant == EP_QUANT_FP8_UE8M0 || quant == EP_QUANT_FP8_UE8M0_MN)
+                                ? 4 * ((G + 3) / 4) : 0;
+    int mn_src = 0, mn_dst = 0;
+    if (quant == EP_QUANT_FP8_UE8M0_MN) {
+        const long long TK = (long long)L.num_tokens * L.num_topk;
+        const long long rows_cap = TK + (TK < E ? TK : E) * (long long)(L.align - 1);
+        mn_src = (int)((rows_cap + 3) / 4 * 4);
+        mn_dst = (cap + 3) / 4 * 4;
+    }
     // Enough warps to keep HBM busy: the valid rows number at most T*K.
     const long long rows_max = (long long)L.num_tokens * L.num_topk;
     long long blocks = (rows_max + kThreads / 32 - 1) / (kThreads / 32);
@@ -77,7 +94,7 @@ cudaError_t launch_masked_repack(const ep_layout_t &L, const void *rows,
     repack_kernel<<<(unsigned)blocks, kThreads, smem, stream>>>(
         static_cast<const uint8_t *>(rows), static_cast<const uint8_t *>(row_scales), row_bytes,
         scale_bytes, L.expert_offset, L.expert_count, E, cap, static_cast<uint8_t *>(slab),
-        static_cast<uint8_t *>(slab_scales), masked_m, L.status);
+        static_cast<uint8_t *>(slab_scales), masked_m, L.status, mn_src, mn_dst);
     return cudaGetLastError();
 }
 

@@ -80,9 +80,15 @@ typedef enum ep_quant {
     EP_QUANT_FP8_F32 = 1,  /* E4M3 rows + fp32 scale per 1x128 group  [rows, H/128]  */
     EP_QUANT_FP8_UE8M0 = 2, /* E4M3 rows + UE8M0 exponent per group, 4 per int32 word
                               [rows, ceil(H/512)]                                   */
-    EP_QUANT_MXFP8 = 3      /* E4M3 rows + E8M0 scale per 1x32 block, 4 per int32 word
+    EP_QUANT_MXFP8 = 3,     /* E4M3 rows + E8M0 scale per 1x32 block, 4 per int32 word
                               [rows, H/128] ([DISC-26563]: 1x32 MXFP8 with dynamic
                               activation scaling; OCP MX v1.0 conversion rule)       */
+    EP_QUANT_FP8_UE8M0_MN = 4 /* as EP_QUANT_FP8_UE8M0, scale words stored MN-major for a
+                              grouped GEMM's TMA: word p of every row contiguous along
+                              the rows, columns padded to 4 rows (16 bytes):
+                              contiguous [P][roundup(rows_capacity, 4)], masked
+                              [E][P][roundup(capacity, 4)], P = ceil(H/512)
+                              ([PR-35634] "Implementation": Blackwell packed UE8M0) */
 } ep_quant_t;
 
 #define EP_MAX_TOPK 32     /* [PR-24443] review: kNumTopk <= 32 */
@@ -135,6 +141,11 @@ int64_t ep_rows_capacity(const ep_layout_t *layout);
  * ceil(H/512) (packed UE8M0), 0 (bf16); -1 if `hidden` is not valid for `quant`. */
 int64_t ep_scale_cols(int32_t hidden, ep_quant_t quant);
 
+/* 32-bit words the scale buffer of `quant` needs for this layout's row space:
+ * rows_capacity * ep_scale_cols for the row-major modes, the padded MN-major
+ * size for EP_QUANT_FP8_UE8M0_MN, 0 for bf16; -1 on a bad layout or hidden. */
+int64_t ep_scale_words(const ep_layout_t *layout, int32_t hidden, ep_quant_t quant);
+
 /* Bytes of device scratch ep_layout() needs for this shape (may be 0).  The
  * scratch holds per-tile expert histograms between the two layout kernels. */
 size_t ep_layout_workspace_bytes(const ep_layout_t *layout);
@@ -174,7 +185,8 @@ ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *layout, void *
  *   out_rows    device [rows, H]: bf16 (EP_QUANT_NONE) or E4M3 bytes; 16-byte
  *               aligned.  Only rows named by dst_row are written; padding rows
  *               and empty slots are left untouched.
- *   out_scales  device [rows, ep_scale_cols(H, quant)] fp32 or int32, 4-byte
+ *   out_scales  device [rows, ep_scale_cols(H, quant)] fp32 or int32 (for
+ *               EP_QUANT_FP8_UE8M0_MN: ep_scale_words() int32, MN-major), 4-byte
  *               aligned; NULL for EP_QUANT_NONE.
  *   topk_w      optional device fp32 [T, K]; with row_w (device fp32 [rows]),
  *               row_w[dst_row[i]] = topk_w[i]. Both NULL to skip.
@@ -220,7 +232,9 @@ ep_status_t ep_combine(const ep_layout_t *layout, const void *y, int32_t hidden,
  *
  *   layout       a CONTIGUOUS layout already filled by ep_layout().
  *   rows         device [rows, H] bf16 or E4M3 (as written by ep_dispatch).
- *   row_scales   device [rows, ep_scale_cols] or NULL for EP_QUANT_NONE.
+ *   row_scales   device [rows, ep_scale_cols] or NULL for EP_QUANT_NONE
+ *                (EP_QUANT_FP8_UE8M0_MN: the contiguous layout's MN-major words,
+ *                and slab_scales receives the masked MN-major layout).
  *   capacity     slab slots per expert, >= 1.
  *   slab         device [E, capacity, H]; slab_scales [E, capacity, cols].
  *   masked_m     device int32 [E] = min(expert_count[e], capacity).

@@ -92,6 +92,10 @@ class Oracle:
         L.orc_dispatch.argtypes = [P, I, I, I, I, P, P, P, P, P]
         L.orc_combine.restype = None
         L.orc_combine.argtypes = [P, P, P, I, I, I, P]
+        L.orc_rank_ids.restype = None
+        L.orc_rank_ids.argtypes = [P, I, I, I, I, P]
+        L.orc_rank_expand.restype = None
+        L.orc_rank_expand.argtypes = [P, I, I, I, I, P, P, I, I, P, P, P, P]
         L.orc_scales_mn_major.restype = None
         L.orc_scales_mn_major.argtypes = [P, I, I, I, I, I, P]
         L.orc_masked_repack.restype = I
@@ -190,6 +194,38 @@ class Oracle:
         self.lib.orc_combine(_p(y), _p(w), _p(d), T, K, H, _p(out))
         return out
 
+    # ------------------------------------------ per-rank deduplicated sending
+    def rank_ids(self, topk_idx: np.ndarray, E: int, R: int) -> np.ndarray:
+        idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+        T, K = idx.shape
+        out = np.zeros((T, K), dtype=np.int32)
+        self.lib.orc_rank_ids(_p(idx), T, K, E, R, _p(out))
+        return out
+
+    def rank_layout(self, topk_idx: np.ndarray, E: int, R: int, align: int = 1):
+        """The rank-major send layout: orc_layout over first-occurrence rank ids."""
+        return self.layout(self.rank_ids(topk_idx, E, R), R, "contig", align=align)
+
+    def rank_expand(self, topk_idx, E, R, send_dst, dst_row, rows, send_rows, send_scales,
+                    fill=0):
+        """Expert-layout rows [rows, ...] filled from the send buffer."""
+        idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+        T, K = idx.shape
+        sr = np.ascontiguousarray(send_rows)
+        out = np.full((rows,) + sr.shape[1:], fill, dtype=sr.dtype)
+        row_bytes = sr.shape[1] * sr.dtype.itemsize if sr.ndim > 1 else sr.dtype.itemsize
+        ss = oscales = None
+        scale_bytes = 0
+        if send_scales is not None:
+            ss = np.ascontiguousarray(send_scales)
+            oscales = np.zeros((rows,) + ss.shape[1:], dtype=ss.dtype)
+            scale_bytes = ss.shape[1] * ss.dtype.itemsize
+        self.lib.orc_rank_expand(_p(idx), T, K, E, R,
+                                 _p(np.ascontiguousarray(send_dst, dtype=np.int32)),
+                                 _p(np.ascontiguousarray(dst_row, dtype=np.int32)),
+                                 row_bytes, scale_bytes, _p(sr), _p(ss), _p(out), _p(oscales))
+        return out, oscales
+
     # ------------------------------------------------- MN-major scale layout
     def scales_mn_major(self, row_major: np.ndarray, layout: str, E: int = 0, cap: int = 0,
                         fill: int = 0) -> np.ndarray:
@@ -239,6 +275,7 @@ def __getattr__(name):
     # module-level convenience: oracle.layout(...) == oracle.default().layout(...)
     if name in ("bf16_round", "bf16_round_array", "bf16_to_float", "e4m3_encode",
                 "e4m3_encode_array", "e4m3_decode", "quant_group", "layout", "dispatch",
-                "combine", "masked_repack", "scales_mn_major"):
+                "combine", "masked_repack", "scales_mn_major", "rank_ids", "rank_layout",
+                "rank_expand"):
         return getattr(default(), name)
     raise AttributeError(name)

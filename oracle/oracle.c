@@ -275,6 +275,69 @@ void orc_combine(const uint16_t *y, const float *topk_w, const int32_t *dst_row,
     }
 }
 
+/* ------------------------------------------ per-rank deduplicated sending */
+
+/* Logical rank r owns experts [r*E/R, (r+1)*E/R).  rank_idx[t*K+k] is the rank
+ * of expert topk_idx[t,k] the first time token t names that rank (ascending
+ * k), -1 for later entries of the same rank and for -1 ids; ids outside
+ * [-1, E) become -2 so that the layout over ranks reports them.  Running
+ * orc_layout on rank_idx with R "experts" then gives the rank-major send
+ * layout: one row per (token, rank) pair, ascending tokens inside a rank. */
+void orc_rank_ids(const int32_t *topk_idx, int T, int K, int E, int R, int32_t *rank_idx) {
+    int per = E / R;
+    for (int t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int e = topk_idx[t * K + k];
+            int out;
+            if (e == -1) {
+                out = -1;
+            } else if (e < -1 || e >= E) {
+                out = -2;
+            } else {
+                int r = e / per;
+                out = r;
+                for (int j = 0; j < k; ++j) {
+                    int ej = topk_idx[t * K + j];
+                    if (ej >= 0 && ej < E && ej / per == r) {
+                        out = -1; /* the rank was named earlier */
+                        break;
+                    }
+                }
+            }
+            rank_idx[t * K + k] = out;
+        }
+    }
+}
+
+/* Local expand: row dst_row[t,k] of the per-expert layout receives the send
+ * row of (t, rank of topk_idx[t,k]), i.e. send_dst[t*K+j] for the first j
+ * naming that rank; the scale row goes along.  Entries with dst_row < 0 are
+ * skipped. */
+void orc_rank_expand(const int32_t *topk_idx, int T, int K, int E, int R,
+                     const int32_t *send_dst, const int32_t *dst_row, int row_bytes,
+                     int scale_bytes, const void *send_rows, const void *send_scales,
+                     void *out_rows, void *out_scales) {
+    int per = E / R;
+    for (int t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int d = dst_row[t * K + k];
+            int e = topk_idx[t * K + k];
+            if (d < 0 || e < 0 || e >= E) continue;
+            int src = -1;
+            for (int j = 0; j <= k && src < 0; ++j) {
+                int ej = topk_idx[t * K + j];
+                if (ej >= 0 && ej < E && ej / per == e / per) src = send_dst[t * K + j];
+            }
+            if (src < 0) continue;
+            memcpy((uint8_t *)out_rows + (size_t)d * row_bytes,
+                   (const uint8_t *)send_rows + (size_t)src * row_bytes, (size_t)row_bytes);
+            if (scale_bytes)
+                memcpy((uint8_t *)out_scales + (size_t)d * scale_bytes,
+                       (const uint8_t *)send_scales + (size_t)src * scale_bytes, (size_t)scale_bytes);
+        }
+    }
+}
+
 /* ------------------------------------------------- MN-major scale layout */
 
 /* Packed UE8M0 scale words re-laid "MN-major" for a grouped GEMM that loads

@@ -19,7 +19,11 @@
  *     conversion rule for the shared scale);
  *   - combine: top-k weighted reduction back to token order (vLLM
  *     tools/ep_kernels commit message, "weighted reduction in combine");
- *   - masked repack: contiguous expert segments -> [E, cap, H] slab.
+ *   - masked repack: contiguous expert segments -> [E, cap, H] slab;
+ *   - per-rank deduplicated send layout and local expand: each token sent once
+ *     to every logical rank owning one of its experts (the V1 dispatch-layout
+ *     pre-pass the first SGLang PR's "Motivation" says V2 folds into dispatch,
+ *     and the vLLM commit's intra/inter-node expert parallelism).
  *
  * Parity pins: every function here is pinned by tests (brute force, closed
  * forms, library cross-checks) except two choices the pages leave open, whose
@@ -66,6 +70,12 @@ void orc_dispatch(const uint16_t *x, int T, int K, int H, int quant,
 
 void orc_combine(const uint16_t *y, const float *topk_w, const int32_t *dst_row,
                  int T, int K, int H, uint16_t *out);
+
+void orc_rank_ids(const int32_t *topk_idx, int T, int K, int E, int R, int32_t *rank_idx);
+void orc_rank_expand(const int32_t *topk_idx, int T, int K, int E, int R,
+                     const int32_t *send_dst, const int32_t *dst_row, int row_bytes,
+                     int scale_bytes, const void *send_rows, const void *send_scales,
+                     void *out_rows, void *out_scales);
 
 void orc_scales_mn_major(const int32_t *row_major, int rows, int P, int masked, int E,
                          int cap, int32_t *out);

@@ -466,7 +466,55 @@ def pin_scales_mn_major(orc, rng):
         assert (grid[:, :, cap:] == -7).all()
 
 
+def pin_rank_dedup(orc, rng):
+    """Send layout by brute force (token t is sent to rank r iff one of its
+    experts lies in r; ascending tokens inside each rank, ranks in order), and
+    expand(dispatch into the send layout) == dispatch into the expert layout."""
+    for it in range(60):
+        T = int(rng.integers(0, 15))
+        R = int(rng.choice([1, 2, 4]))
+        E = R * int(rng.integers(1, 4))
+        K = int(rng.integers(1, 5))
+        idx = rng.integers(-1, E, size=(T, K)).astype(np.int32)
+        RL = orc.rank_layout(idx, E, R, align=1)
+        ranks = [set() if T else set() for _ in range(T)]
+        for t in range(T):
+            ranks[t] = {int(e) * R // E for e in idx[t] if e >= 0}
+        counts = [sum(1 for t in range(T) if r in ranks[t]) for r in range(R)]
+        assert list(RL["count"]) == counts
+        expect_row = {}
+        row = 0
+        for r in range(R):
+            for t in range(T):
+                if r in ranks[t]:
+                    expect_row[(t, r)] = row
+                    row += 1
+        assert RL["rows"] == row
+        for t in range(T):
+            seen = set()
+            for k in range(K):
+                e = idx[t, k]
+                d = RL["dst_row"][t, k]
+                if e < 0 or (e * R // E) in seen:
+                    assert d == -1
+                else:
+                    seen.add(e * R // E)
+                    assert d == expect_row[(t, e * R // E)]
+        # composition: expand(send) == direct dispatch, for every quantisation
+        H = 256
+        x = torch_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+        L = orc.layout(idx, E, "contig", align=4)
+        for quant in ("none", "fp8_ue8m0", "mxfp8"):
+            srows, ssc, _ = orc.dispatch(x, RL["dst_row"], RL["rows"], quant)
+            drows, dsc, _ = orc.dispatch(x, L["dst_row"], L["rows"], quant, fill=3)
+            erows, esc = orc.rank_expand(idx, E, R, RL["dst_row"], L["dst_row"], L["rows"],
+                                         srows, ssc, fill=3)
+            assert np.array_equal(erows, drows)
+            if dsc is not None:
+                assert np.array_equal(esc, dsc)
+
+
 ALL_PINS = [pin_bf16, pin_e4m3_decode, pin_e4m3_roundtrip_and_ties, pin_e4m3_nearest,
             pin_quant_f32, pin_quant_ue8m0, pin_quant_mx, pin_layout_bruteforce, pin_layout_bad_ids,
             pin_dispatch, pin_combine, pin_masked_repack, pin_fp8_roundtrip,
-            pin_scales_mn_major]
+            pin_scales_mn_major, pin_rank_dedup]

@@ -30,6 +30,8 @@ MUTANTS = {
                              "memcpy((uint8_t *)out_scales + (size_t)dst * (H / 32), mx + (H > 32), (size_t)(H / 32 - (H > 32)));"),
     "mn_major_unaligned": ("int rows4 = (rows + 3) / 4 * 4;", "int rows4 = rows;"),
     "mn_major_swapped": ("out[((size_t)e * P + p) * cap4 + s]", "out[((size_t)p * E + e) * cap4 + s]"),
+    "rank_no_dedup": ("                        out = -1; /* the rank was named earlier */", "                        out = r;"),
+    "rank_expand_wrong_source": ("for (int j = 0; j <= k && src < 0; ++j)", "for (int j = k; j <= k && src < 0; ++j)"),
     "layout_no_padding": ("offset[e] + round_up(count[e], align)", "offset[e] + count[e]"),
     "layout_k_descending": ("for (int k = 0; k < K; ++k) {\n            int i = t * K + k;",
                             "for (int k = K - 1; k >= 0; --k) {\n            int i = t * K + k;"),
