@@ -379,6 +379,7 @@ def run_ours(args, w):
     if not args.skip_decode:
         line["dispatch_variants"] = measure_dispatch_variants(ep, w, L, x_d, dev)
         line["decode"] = measure_decode(ep, dev)
+        line["rank_dedup"] = measure_rank_dedup(ep, dev)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, idx, wts, x)
     print(json.dumps(line), flush=True)
@@ -506,6 +507,52 @@ def measure_dispatch_variants(ep, w, L, x_d, dev, reps=20):
                       "tokens_per_s": round(w.T / (us * 1e-6), 1)}
         del out_rows, sc
     return res
+
+
+def measure_rank_dedup(ep, dev, reps=20):
+    """Per-rank deduplicated sending at the Zipf workload (8 logical ranks):
+    rank layout + dispatch into the send buffer + local expand, beside the
+    direct dispatch of the same tokens."""
+    import torch
+    w = workloads.CONFIGS["skewed_zipf"]
+    idx, wts, x = workloads.make_inputs(w)
+    idx_d = torch.from_numpy(idx).to(dev)
+    x_d = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    L = ep.ep_layout(idx_d, w.E, align=w.align, num_ranks=w.R)
+    RL, rank_idx = ep.ep_rank_layout(idx_d, w.E, w.R)
+    send_rows, _, _ = ep.ep_dispatch(RL, x_d, w.quant)
+    out_rows, _ = ep.ep_rank_expand(RL, L, idx_d, w.quant, send_rows, None)
+    direct, _, _ = ep.ep_dispatch(L, x_d, w.quant)
+    torch.cuda.synchronize()
+    send_n = int(RL.expert_offset[-1].item())
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+    t_rl = timed(lambda: ep.ep_rank_layout(idx_d, w.E, w.R, out=RL, rank_idx=rank_idx))
+    t_send = timed(lambda: ep.ep_dispatch(RL, x_d, w.quant, out_rows=send_rows))
+    t_exp = timed(lambda: ep.ep_rank_expand(RL, L, idx_d, w.quant, send_rows, None,
+                                            out_rows=out_rows))
+    t_direct = timed(lambda: ep.ep_dispatch(L, x_d, w.quant, out_rows=direct))
+    row = 2 * w.H
+    send_bytes = w.T * row + send_n * row + w.T * w.K * 4
+    exp_bytes = send_n * row + w.T * w.K * row + 2 * w.T * w.K * 4
+    return {"workload": w.name, "ranks": w.R, "send_rows": send_n,
+            "rows_per_token": round(send_n / w.T, 3),
+            "rank_layout_us": round(t_rl, 2),
+            "send_dispatch_us": round(t_send, 2),
+            "send_dispatch_GBps": round(send_bytes / (t_send * 1e-6) / 1e9, 1),
+            "expand_us": round(t_exp, 2),
+            "expand_GBps": round(exp_bytes / (t_exp * 1e-6) / 1e9, 1),
+            "direct_dispatch_us": round(t_direct, 2)}
 
 
 def measure_e2e(ep, w, L, idx, wts, x, y_dev, out_rows, out_scales, dev, stream, args):

@@ -53,7 +53,8 @@ _lib = None
 
 EXPORTS = ("ep_status_str", "ep_rows_capacity", "ep_scale_cols", "ep_scale_words",
            "ep_layout_workspace_bytes",
-           "ep_layout", "ep_dispatch", "ep_combine", "ep_masked_repack", "ep_layout_noalloc")
+           "ep_layout", "ep_dispatch", "ep_combine", "ep_masked_repack", "ep_layout_noalloc",
+           "ep_rank_layout", "ep_rank_expand")
 NOALLOC_SCRATCH_BYTES = 256 * 1024
 
 
@@ -86,6 +87,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ep_combine.argtypes = [LP, P, I32, P, P, P]
     L.ep_masked_repack.restype = ctypes.c_int
     L.ep_masked_repack.argtypes = [LP, P, P, I32, ctypes.c_int, I32, P, P, P, P]
+    L.ep_rank_layout.restype = ctypes.c_int
+    L.ep_rank_layout.argtypes = [P, I32, P, LP, P, SZ, P]
+    L.ep_rank_expand.restype = ctypes.c_int
+    L.ep_rank_expand.argtypes = [LP, LP, P, I32, ctypes.c_int, P, P, P, P, P]
     L.ep_layout_noalloc.restype = ctypes.c_int
     L.ep_layout_noalloc.argtypes = [P, LP, P]
     if path == LIB_PATH:
@@ -343,3 +348,44 @@ def ep_layout_noalloc(topk_idx: torch.Tensor, out: Layout, stream=None) -> Layou
                                             ctypes.byref(out.struct()), _stream(stream))
     _check(code, "ep_layout_noalloc")
     return out
+
+
+def ep_rank_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, align: int = 1,
+                   out: Optional[Layout] = None, rank_idx: Optional[torch.Tensor] = None,
+                   stream=None):
+    """Per-rank deduplicated send layout; returns (rank Layout, rank_idx [T, K])."""
+    if topk_idx.dtype != torch.int32 or topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be int32 [T, K]")
+    T, K = topk_idx.shape
+    RL = out if out is not None else new_layout(T, K, num_ranks, "contig", align=align,
+                                                device=topk_idx.device)
+    if rank_idx is None:
+        rank_idx = torch.empty((T, K), dtype=torch.int32, device=topk_idx.device)
+    ws = RL.workspace
+    code = load_library().ep_rank_layout(_ptr(topk_idx) if T * K else None, num_experts,
+                                         _ptr(rank_idx) if T * K else None,
+                                         ctypes.byref(RL.struct()), _ptr(ws),
+                                         ws.numel() * 4 if ws is not None else 0, _stream(stream))
+    _check(code, "ep_rank_layout")
+    return RL, rank_idx
+
+
+def ep_rank_expand(rank_layout: Layout, layout: Layout, topk_idx: torch.Tensor, quant: str,
+                   send_rows: torch.Tensor, send_scales: Optional[torch.Tensor],
+                   out_rows: Optional[torch.Tensor] = None,
+                   out_scales: Optional[torch.Tensor] = None, stream=None):
+    """Send buffer -> per-expert rows (and scale rows); returns (out_rows, out_scales)."""
+    H = send_rows.shape[-1]
+    dev = send_rows.device
+    rows = layout.rows_capacity
+    if out_rows is None:
+        out_rows = torch.empty((max(rows, 1), H), device=dev, dtype=send_rows.dtype)
+    if send_scales is not None and out_scales is None:
+        out_scales = torch.empty((max(rows, 1), send_scales.shape[-1]), device=dev,
+                                 dtype=send_scales.dtype)
+    code = load_library().ep_rank_expand(ctypes.byref(rank_layout.struct()),
+                                         ctypes.byref(layout.struct()), _ptr(topk_idx), H,
+                                         QUANT[quant], _ptr(send_rows), _ptr(send_scales),
+                                         _ptr(out_rows), _ptr(out_scales), _stream(stream))
+    _check(code, "ep_rank_expand")
+    return out_rows, out_scales

@@ -183,4 +183,52 @@ ep_status_t ep_masked_repack(const ep_layout_t *L, const void *rows, const void 
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_rank_layout(const int32_t *topk_idx, int32_t num_experts, int32_t *rank_idx,
+                           const ep_layout_t *RL, void *workspace, size_t workspace_bytes,
+                           ep_stream_t stream) {
+    ep_status_t st = check_layout(RL);
+    if (st != EP_OK) return st;
+    if (RL->kind != EP_LAYOUT_CONTIG) return EP_ERR_INVALID_ARG;
+    if (num_experts < RL->num_experts || num_experts > EP_MAX_EXPERTS ||
+        num_experts % RL->num_experts != 0)
+        return EP_ERR_INVALID_ARG;
+    const int TK = RL->num_tokens * RL->num_topk;
+    if (TK > 0 && (!topk_idx || !rank_idx || !aligned(topk_idx, 4) || !aligned(rank_idx, 4)))
+        return EP_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err = launch_rank_ids(topk_idx, RL->num_tokens, RL->num_topk, num_experts,
+                                      RL->num_experts, rank_idx, s);
+    if (err != cudaSuccess) return EP_ERR_CUDA;
+    return ep_layout(rank_idx, RL, workspace, workspace_bytes, stream);
+}
+
+ep_status_t ep_rank_expand(const ep_layout_t *RL, const ep_layout_t *L, const int32_t *topk_idx,
+                           int32_t hidden, ep_quant_t quant, const void *send_rows,
+                           const void *send_scales, void *out_rows, void *out_scales,
+                           ep_stream_t stream) {
+    ep_status_t st = check_layout(RL);
+    if (st != EP_OK) return st;
+    st = check_layout(L);
+    if (st != EP_OK) return st;
+    st = check_hidden(hidden, quant);
+    if (st != EP_OK) return st;
+    if (quant == EP_QUANT_FP8_UE8M0_MN) return EP_ERR_UNSUPPORTED;  // row-major scales only
+    if (RL->num_tokens != L->num_tokens || RL->num_topk != L->num_topk ||
+        L->num_experts % RL->num_experts != 0)
+        return EP_ERR_INVALID_ARG;
+    if (L->num_tokens == 0) return EP_OK;
+    if (!topk_idx || !send_rows || !out_rows || !aligned(send_rows, 16) || !aligned(out_rows, 16))
+        return EP_ERR_INVALID_ARG;
+    const int G = hidden / 128;
+    const int row_bytes = quant == EP_QUANT_NONE ? 2 * hidden : hidden;
+    const int scale_bytes = (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_MXFP8) ? 4 * G
+                            : quant == EP_QUANT_FP8_UE8M0 ? 4 * ((G + 3) / 4) : 0;
+    if (scale_bytes && (!send_scales || !out_scales || !aligned(send_scales, 4) ||
+                        !aligned(out_scales, 4)))
+        return EP_ERR_INVALID_ARG;
+    return from_cuda(launch_rank_expand(*RL, *L, topk_idx, row_bytes, scale_bytes, send_rows,
+                                        send_scales, out_rows, out_scales,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

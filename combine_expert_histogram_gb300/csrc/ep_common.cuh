@@ -134,4 +134,11 @@ cudaError_t launch_masked_repack(const ep_layout_t &L, const void *rows,
                                  void *slab, void *slab_scales, int32_t *masked_m,
                                  cudaStream_t stream);
 
+cudaError_t launch_rank_ids(const int32_t *topk_idx, int T, int K, int E, int R,
+                            int32_t *rank_idx, cudaStream_t stream);
+cudaError_t launch_rank_expand(const ep_layout_t &rank_layout, const ep_layout_t &layout,
+                               const int32_t *topk_idx, int row_bytes, int scale_bytes,
+                               const void *send_rows, const void *send_scales, void *out_rows,
+                               void *out_scales, cudaStream_t stream);
+
 }  // namespace ep

@@ -249,6 +249,43 @@ ep_status_t ep_masked_repack(const ep_layout_t *layout, const void *rows,
                              int32_t *masked_m, ep_stream_t stream);
 
 /*
+ * ep_rank_layout -- per-logical-rank deduplicated send layout: a token is sent
+ * once to every logical rank owning one of its experts (the dispatch-layout
+ * pre-pass [PR-24443] "Motivation" says V2 infers internally; [VLLM-EP]
+ * intra/inter-node expert parallelism).  Rank r owns experts
+ * [r*E/R, (r+1)*E/R).
+ *
+ *   topk_idx     device int32 [T, K] expert ids (E = num_experts).
+ *   rank_idx     device int32 [T*K], written: the rank of entry (t,k) if no
+ *                earlier k of token t named that rank, else -1 (-2 for ids
+ *                outside [-1, E), reported as EP_ERR_BAD_EXPERT_ID).
+ *   rank_layout  a contiguous ep_layout_t with num_experts = R (R divides E),
+ *                num_tokens = T, num_topk = K, filled as ep_layout() fills it
+ *                from rank_idx: dst_row[t*K+k] is the send row of (t, rank) at
+ *                the entry that first names the rank, expert_count[r] the
+ *                tokens sent to rank r, expert_offset the rank-major segments
+ *                (ascending tokens inside a rank), row_src the entry per row.
+ *   workspace    as for ep_layout() with rank_layout's shape.
+ * ep_dispatch(rank_layout, ...) then writes each token once per rank.
+ */
+ep_status_t ep_rank_layout(const int32_t *topk_idx, int32_t num_experts, int32_t *rank_idx,
+                           const ep_layout_t *rank_layout, void *workspace,
+                           size_t workspace_bytes, ep_stream_t stream);
+
+/*
+ * ep_rank_expand -- the receiving side's local expand: row dst_row[t,k] of
+ * `layout` (the per-expert layout of the same topk_idx) receives the send row
+ * of (t, rank of topk_idx[t,k]), with its scale row.  quant is the mode the
+ * send buffer was dispatched with; the MN-major scale layout is not
+ * supported here (EP_ERR_UNSUPPORTED).  Rows dst_row < 0 are skipped.
+ * expand(dispatch(rank_layout, x)) equals dispatch(layout, x) byte for byte.
+ */
+ep_status_t ep_rank_expand(const ep_layout_t *rank_layout, const ep_layout_t *layout,
+                           const int32_t *topk_idx, int32_t hidden, ep_quant_t quant,
+                           const void *send_rows, const void *send_scales, void *out_rows,
+                           void *out_scales, ep_stream_t stream);
+
+/*
  * ep_layout_noalloc -- ep_layout with its scratch taken from a fixed array
  * inside the library, for callers that cannot allocate device memory (a
  * serving runtime that reserves all memory at start-up and forbids later
