@@ -92,6 +92,8 @@ class Oracle:
         L.orc_dispatch.argtypes = [P, I, I, I, I, P, P, P, P, P]
         L.orc_combine.restype = None
         L.orc_combine.argtypes = [P, P, P, I, I, I, P]
+        L.orc_route_topk.restype = None
+        L.orc_route_topk.argtypes = [P, P, I, I, I, I, I, I, P, P, P]
         L.orc_rank_ids.restype = None
         L.orc_rank_ids.argtypes = [P, I, I, I, I, P]
         L.orc_rank_expand.restype = None
@@ -194,6 +196,21 @@ class Oracle:
         self.lib.orc_combine(_p(y), _p(w), _p(d), T, K, H, _p(out))
         return out
 
+    # ------------------------------------------------------------ router top-k
+    def route_topk(self, logits: np.ndarray, K: int, mode: str = "softmax",
+                   bias: np.ndarray | None = None, n_group: int = 1, topk_group: int = 1):
+        """(topk_idx int32 [T,K], topk_w float64 [T,K], selection score fp32 [T,K])."""
+        lg = np.ascontiguousarray(logits, dtype=np.float32)
+        T, E = lg.shape
+        idx = np.zeros((T, K), dtype=np.int32)
+        w = np.zeros((T, K), dtype=np.float64)
+        sc = np.zeros((T, K), dtype=np.float32)
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        m = {"softmax": 0, "grouped_sigmoid": 1}[mode]
+        self.lib.orc_route_topk(_p(lg), _p(b), T, E, K, m, n_group, topk_group, _p(idx),
+                                _p(w), _p(sc))
+        return idx, w, sc
+
     # ------------------------------------------ per-rank deduplicated sending
     def rank_ids(self, topk_idx: np.ndarray, E: int, R: int) -> np.ndarray:
         idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
@@ -276,6 +293,6 @@ def __getattr__(name):
     if name in ("bf16_round", "bf16_round_array", "bf16_to_float", "e4m3_encode",
                 "e4m3_encode_array", "e4m3_decode", "quant_group", "layout", "dispatch",
                 "combine", "masked_repack", "scales_mn_major", "rank_ids", "rank_layout",
-                "rank_expand"):
+                "rank_expand", "route_topk"):
         return getattr(default(), name)
     raise AttributeError(name)

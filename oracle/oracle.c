@@ -275,6 +275,97 @@ void orc_combine(const uint16_t *y, const float *topk_w, const int32_t *dst_row,
     }
 }
 
+/* ------------------------------------------------------------ router top-k */
+
+/* Is (va, a) ranked before (vb, b)?  Larger value first, lower index on ties. */
+static int ranks_before(double va, int a, double vb, int b) { return va > vb || (va == vb && a < b); }
+
+/* Top-K selection by repeated maximum over `score` (entries with keep[e] == 0
+ * are excluded); writes the chosen indices in rank order. */
+static void select_top(const double *score, const int *keep, int n, int k, int *out) {
+    int *taken = (int *)calloc((size_t)(n > 0 ? n : 1), sizeof(int));
+    for (int j = 0; j < k; ++j) {
+        int best = -1;
+        for (int e = 0; e < n; ++e) {
+            if (taken[e] || (keep && !keep[e])) continue;
+            if (best < 0 || ranks_before(score[e], e, score[best], best)) best = e;
+        }
+        out[j] = best;
+        if (best >= 0) taken[best] = 1;
+    }
+    free(taken);
+}
+
+/* Router output for T tokens of E logits.
+ *   SOFTMAX: p = softmax(logits); topk_idx = the K largest p (ties to the lower
+ *     expert id; p is monotone in the logit, so the logits decide);
+ *     topk_w = p_sel / sum(p_sel).
+ *   GROUPED_SIGMOID (DeepSeek-V3 style): s = sigmoid(logit), c = s + bias, the
+ *     selection score, computed in fp32 (the precision the decision is taken
+ *     in); experts split into n_group groups of E/n_group; group score = sum
+ *     of its two largest c; the topk_group best groups are kept (ties to the
+ *     lower group id); topk_idx = the K largest c among kept experts;
+ *     topk_w = s_sel / sum(s_sel).
+ * Weights are computed in fp64.  sel_score[t*K+j] is the fp32 selection score
+ * of the j-th pick (logit, or c), for tie analysis in tests. */
+void orc_route_topk(const float *logits, const float *bias, int T, int E, int K, int mode,
+                    int n_group, int topk_group, int32_t *topk_idx, double *topk_w,
+                    float *sel_score) {
+    double *score = (double *)malloc(sizeof(double) * (size_t)E);
+    double *sig = (double *)malloc(sizeof(double) * (size_t)E);
+    float *c32 = (float *)malloc(sizeof(float) * (size_t)E);
+    int *keep = (int *)malloc(sizeof(int) * (size_t)E);
+    int *pick = (int *)malloc(sizeof(int) * (size_t)(K > 0 ? K : 1));
+    for (int t = 0; t < T; ++t) {
+        const float *l = logits + (size_t)t * E;
+        if (mode == ORC_ROUTE_SOFTMAX) {
+            double m = -INFINITY, z = 0.0;
+            for (int e = 0; e < E; ++e) m = l[e] > m ? l[e] : m;
+            for (int e = 0; e < E; ++e) {
+                sig[e] = exp((double)l[e] - m);  /* unnormalised softmax */
+                z += sig[e];
+                score[e] = l[e];
+            }
+            for (int e = 0; e < E; ++e) sig[e] /= z;
+            select_top(score, NULL, E, K, pick);
+        } else {
+            int gs = E / n_group;
+            for (int e = 0; e < E; ++e) {
+                float s32 = 1.0f / (1.0f + expf(-l[e]));
+                c32[e] = s32 + (bias ? bias[e] : 0.0f);
+                sig[e] = 1.0 / (1.0 + exp(-(double)l[e]));
+                score[e] = c32[e];
+            }
+            double *gscore = (double *)malloc(sizeof(double) * (size_t)n_group);
+            int *gpick = (int *)malloc(sizeof(int) * (size_t)n_group);
+            for (int g = 0; g < n_group; ++g) {
+                int two[2];
+                select_top(score + (size_t)g * gs, NULL, gs, 2, two);
+                gscore[g] = (double)((float)score[g * gs + two[0]] + (float)score[g * gs + two[1]]);
+            }
+            select_top(gscore, NULL, n_group, topk_group, gpick);
+            for (int e = 0; e < E; ++e) keep[e] = 0;
+            for (int j = 0; j < topk_group; ++j)
+                for (int e = gpick[j] * gs; e < (gpick[j] + 1) * gs; ++e) keep[e] = 1;
+            select_top(score, keep, E, K, pick);
+            free(gscore);
+            free(gpick);
+        }
+        double sum = 0.0;
+        for (int j = 0; j < K; ++j) sum += sig[pick[j]];
+        for (int j = 0; j < K; ++j) {
+            topk_idx[t * K + j] = pick[j];
+            topk_w[t * K + j] = sig[pick[j]] / sum;
+            if (sel_score) sel_score[t * K + j] = (float)score[pick[j]];
+        }
+    }
+    free(score);
+    free(sig);
+    free(c32);
+    free(keep);
+    free(pick);
+}
+
 /* ------------------------------------------ per-rank deduplicated sending */
 
 /* Logical rank r owns experts [r*E/R, (r+1)*E/R).  rank_idx[t*K+k] is the rank

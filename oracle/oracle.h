@@ -20,6 +20,11 @@
  *   - combine: top-k weighted reduction back to token order (vLLM
  *     tools/ep_kernels commit message, "weighted reduction in combine");
  *   - masked repack: contiguous expert segments -> [E, cap, H] slab;
+ *   - router top-k before the layout (softmax top-K renormalised; DeepSeek-V3
+ *     style grouped sigmoid with bias), the step whose output topk_idx V2
+ *     dispatch takes (first SGLang PR, "Motivation"); no page gives its
+ *     formulas, so it follows the model families the second PR's "Supported
+ *     scope" names;
  *   - per-rank deduplicated send layout and local expand: each token sent once
  *     to every logical rank owning one of its experts (the V1 dispatch-layout
  *     pre-pass the first SGLang PR's "Motivation" says V2 folds into dispatch,
@@ -76,6 +81,12 @@ void orc_rank_expand(const int32_t *topk_idx, int T, int K, int E, int R,
                      const int32_t *send_dst, const int32_t *dst_row, int row_bytes,
                      int scale_bytes, const void *send_rows, const void *send_scales,
                      void *out_rows, void *out_scales);
+
+#define ORC_ROUTE_SOFTMAX 0
+#define ORC_ROUTE_GROUPED_SIGMOID 1
+void orc_route_topk(const float *logits, const float *bias, int T, int E, int K, int mode,
+                    int n_group, int topk_group, int32_t *topk_idx, double *topk_w,
+                    float *sel_score);
 
 void orc_scales_mn_major(const int32_t *row_major, int rows, int P, int masked, int E,
                          int cap, int32_t *out);

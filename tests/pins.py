@@ -514,7 +514,43 @@ def pin_rank_dedup(orc, rng):
                 assert np.array_equal(esc, dsc)
 
 
+def pin_route_topk(orc, rng):
+    """Router top-k against numpy/scipy restatements: stable argsort of the logits
+    (softmax is monotone), scipy's softmax / expit for the weights, and the grouped
+    selection written out with numpy in fp32; exact ties go to the lower id."""
+    import scipy.special as sp
+    for T, E, K in ((64, 8, 2), (40, 32, 5), (20, 16, 16)):
+        lg = rng.standard_normal((T, E)).astype(np.float32)
+        lg[:T // 2] = np.round(lg[:T // 2], 1)  # many exact ties
+        idx, w, _ = orc.route_topk(lg, K, "softmax")
+        exp_idx = np.argsort(-lg.astype(np.float64), axis=1, kind="stable")[:, :K]
+        assert np.array_equal(idx, exp_idx)
+        p = sp.softmax(lg.astype(np.float64), axis=1)
+        sel = np.take_along_axis(p, exp_idx, axis=1)
+        assert np.allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-12, atol=0)
+    for T, E, K, G, TG in ((50, 32, 4, 4, 2), (30, 64, 8, 8, 4), (10, 16, 3, 2, 1)):
+        lg = rng.standard_normal((T, E)).astype(np.float32)
+        lg[::3, :] = np.round(lg[::3, :])  # exact ties within groups
+        bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+        idx, w, _ = orc.route_topk(lg, K, "grouped_sigmoid", bias=bias, n_group=G, topk_group=TG)
+        s32 = (np.float32(1.0) / (np.float32(1.0) + np.exp(-lg))).astype(np.float32)
+        c = (s32 + bias).astype(np.float32)
+        gs = E // G
+        top2 = -np.sort(-c.reshape(T, G, gs), axis=2)[:, :, :2]
+        gscore = (top2[:, :, 0] + top2[:, :, 1]).astype(np.float32)
+        keep_g = np.argsort(-gscore.astype(np.float64), axis=1, kind="stable")[:, :TG]
+        mask = np.zeros((T, G), dtype=bool)
+        np.put_along_axis(mask, keep_g, True, axis=1)
+        cm = np.where(np.repeat(mask, gs, axis=1), c.astype(np.float64), -np.inf)
+        exp_idx = np.argsort(-cm, axis=1, kind="stable")[:, :K]
+        assert np.array_equal(idx, exp_idx)
+        assert np.isin(idx // gs, keep_g).all()  # every pick lies in a kept group
+        sg = sp.expit(lg.astype(np.float64))
+        sel = np.take_along_axis(sg, exp_idx, axis=1)
+        assert np.allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-12, atol=0)
+
+
 ALL_PINS = [pin_bf16, pin_e4m3_decode, pin_e4m3_roundtrip_and_ties, pin_e4m3_nearest,
             pin_quant_f32, pin_quant_ue8m0, pin_quant_mx, pin_layout_bruteforce, pin_layout_bad_ids,
             pin_dispatch, pin_combine, pin_masked_repack, pin_fp8_roundtrip,
-            pin_scales_mn_major, pin_rank_dedup]
+            pin_scales_mn_major, pin_rank_dedup, pin_route_topk]

@@ -32,6 +32,11 @@ MUTANTS = {
     "mn_major_swapped": ("out[((size_t)e * P + p) * cap4 + s]", "out[((size_t)p * E + e) * cap4 + s]"),
     "rank_no_dedup": ("                        out = -1; /* the rank was named earlier */", "                        out = r;"),
     "rank_expand_wrong_source": ("for (int j = 0; j <= k && src < 0; ++j)", "for (int j = k; j <= k && src < 0; ++j)"),
+    "route_ties_high": ("return va > vb || (va == vb && a < b);", "return va > vb || (va == vb && a > b);"),
+    "route_group_top1": ("gscore[g] = (double)((float)score[g * gs + two[0]] + (float)score[g * gs + two[1]]);",
+                         "gscore[g] = (double)((float)score[g * gs + two[0]]);"),
+    "route_no_renorm": ("topk_w[t * K + j] = sig[pick[j]] / sum;", "topk_w[t * K + j] = sig[pick[j]];"),
+    "route_no_bias": ("c32[e] = s32 + (bias ? bias[e] : 0.0f);", "c32[e] = s32;"),
     "layout_no_padding": ("offset[e] + round_up(count[e], align)", "offset[e] + count[e]"),
     "layout_k_descending": ("for (int k = 0; k < K; ++k) {\n            int i = t * K + k;",
                             "for (int k = K - 1; k >= 0; --k) {\n            int i = t * K + k;"),
