@@ -380,6 +380,7 @@ def run_ours(args, w):
         line["dispatch_variants"] = measure_dispatch_variants(ep, w, L, x_d, dev)
         line["decode"] = measure_decode(ep, dev)
         line["rank_dedup"] = measure_rank_dedup(ep, dev)
+        line["router"] = measure_router(ep, dev)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, idx, wts, x)
     print(json.dumps(line), flush=True)
@@ -506,6 +507,40 @@ def measure_dispatch_variants(ep, w, L, x_d, dev, reps=20):
         res[quant] = {"us": round(us, 2), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                       "tokens_per_s": round(w.T / (us * 1e-6), 1)}
         del out_rows, sc
+    return res
+
+
+def measure_router(ep, dev, reps=20):
+    """ep_route_topk at the two router families' bench shapes (fp32 logits)."""
+    import torch
+    res = {}
+    for name, T, E, K, mode, G, TG in (("dsv3_prefill", 16384, 256, 8, "grouped_sigmoid", 8, 4),
+                                       ("dsv3_decode", 1024, 256, 8, "grouped_sigmoid", 8, 4),
+                                       ("qwen3_30b_a3b_decode", 256, 128, 8, "softmax", 1, 1)):
+        g = torch.Generator(device=dev)
+        g.manual_seed(11)
+        lg = torch.randn((T, E), generator=g, device=dev, dtype=torch.float32)
+        bias = torch.randn(E, generator=g, device=dev, dtype=torch.float32) * 0.1
+        idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+        wts = torch.empty((T, K), dtype=torch.float32, device=dev)
+
+        def run():
+            ep.ep_route_topk(lg, K, mode, bias=bias, n_group=G, topk_group=TG, topk_idx=idx,
+                             topk_w=wts)
+
+        for _ in range(3):
+            run()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            run()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        nbytes = T * E * 4 + E * 4 + T * K * 8
+        res[name] = {"mode": mode, "T": T, "E": E, "K": K, "us": round(us, 2),
+                     "tokens_per_s": round(T / (us * 1e-6), 1),
+                     "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1)}
     return res
 
 

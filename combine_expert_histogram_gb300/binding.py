@@ -54,7 +54,7 @@ _lib = None
 EXPORTS = ("ep_status_str", "ep_rows_capacity", "ep_scale_cols", "ep_scale_words",
            "ep_layout_workspace_bytes",
            "ep_layout", "ep_dispatch", "ep_combine", "ep_masked_repack", "ep_layout_noalloc",
-           "ep_rank_layout", "ep_rank_expand")
+           "ep_rank_layout", "ep_rank_expand", "ep_route_topk")
 NOALLOC_SCRATCH_BYTES = 256 * 1024
 
 
@@ -87,6 +87,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ep_combine.argtypes = [LP, P, I32, P, P, P]
     L.ep_masked_repack.restype = ctypes.c_int
     L.ep_masked_repack.argtypes = [LP, P, P, I32, ctypes.c_int, I32, P, P, P, P]
+    L.ep_route_topk.restype = ctypes.c_int
+    L.ep_route_topk.argtypes = [P, P, I32, I32, I32, ctypes.c_int, I32, I32, P, P, P]
     L.ep_rank_layout.restype = ctypes.c_int
     L.ep_rank_layout.argtypes = [P, I32, P, LP, P, SZ, P]
     L.ep_rank_expand.restype = ctypes.c_int
@@ -389,3 +391,26 @@ def ep_rank_expand(rank_layout: Layout, layout: Layout, topk_idx: torch.Tensor, 
                                          _ptr(out_rows), _ptr(out_scales), _stream(stream))
     _check(code, "ep_rank_expand")
     return out_rows, out_scales
+
+
+ROUTE = {"softmax": 0, "grouped_sigmoid": 1}
+
+
+def ep_route_topk(logits: torch.Tensor, num_topk: int, mode: str = "softmax",
+                  bias: Optional[torch.Tensor] = None, n_group: int = 1, topk_group: int = 1,
+                  topk_idx: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None,
+                  stream=None):
+    """Router top-k from fp32 logits [T, E]; returns (topk_idx int32, topk_w fp32) [T, K]."""
+    if logits.dtype != torch.float32 or logits.dim() != 2:
+        raise ValueError("logits must be fp32 [T, E]")
+    T, E = logits.shape
+    dev = logits.device
+    if topk_idx is None:
+        topk_idx = torch.empty((T, num_topk), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, num_topk), dtype=torch.float32, device=dev)
+    code = load_library().ep_route_topk(_ptr(logits), _ptr(bias), T, E, num_topk, ROUTE[mode],
+                                        n_group, topk_group, _ptr(topk_idx), _ptr(topk_w),
+                                        _stream(stream))
+    _check(code, "ep_route_topk")
+    return topk_idx, topk_w

@@ -19,8 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libep.so")
 
-SOURCES = ["abi.cu", "layout.cu", "dispatch.cu", "combine.cu", "repack.cu", "rank.cu",
-           "noalloc.cu"]
+SOURCES = ["abi.cu", "route.cu", "layout.cu", "dispatch.cu", "combine.cu", "repack.cu",
+           "rank.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr"]

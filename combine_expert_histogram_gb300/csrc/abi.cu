@@ -183,6 +183,28 @@ ep_status_t ep_masked_repack(const ep_layout_t *L, const void *rows, const void 
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_route_topk(const float *logits, const float *bias, int32_t T, int32_t E,
+                          int32_t K, ep_route_t mode, int32_t n_group, int32_t topk_group,
+                          int32_t *topk_idx, float *topk_w, ep_stream_t stream) {
+    if (T < 0 || E < 1 || E > EP_MAX_EXPERTS || K < 1 || K > EP_MAX_TOPK || K > E)
+        return EP_ERR_INVALID_ARG;
+    if (mode == EP_ROUTE_GROUPED_SIGMOID) {
+        if (n_group < 1 || n_group > 32 || E % n_group != 0 || E / n_group < 2 ||
+            topk_group < 1 || topk_group > n_group || K > topk_group * (E / n_group))
+            return EP_ERR_INVALID_ARG;
+    } else if (mode != EP_ROUTE_SOFTMAX) {
+        return EP_ERR_INVALID_ARG;
+    }
+    if ((int64_t)T * E > INT_MAX) return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+    if (!logits || !topk_idx || !topk_w || !aligned(logits, 4) || !aligned(topk_idx, 4) ||
+        !aligned(topk_w, 4) || !aligned(bias, 4))
+        return EP_ERR_INVALID_ARG;
+    return from_cuda(launch_route(logits, mode == EP_ROUTE_GROUPED_SIGMOID ? bias : nullptr, T, E,
+                                  K, (int)mode, n_group, topk_group, topk_idx, topk_w,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 ep_status_t ep_rank_layout(const int32_t *topk_idx, int32_t num_experts, int32_t *rank_idx,
                            const ep_layout_t *RL, void *workspace, size_t workspace_bytes,
                            ep_stream_t stream) {

@@ -134,6 +134,9 @@ cudaError_t launch_masked_repack(const ep_layout_t &L, const void *rows,
                                  void *slab, void *slab_scales, int32_t *masked_m,
                                  cudaStream_t stream);
 
+cudaError_t launch_route(const float *logits, const float *bias, int T, int E, int K, int mode,
+                         int n_group, int topk_group, int32_t *topk_idx, float *topk_w,
+                         cudaStream_t stream);
 cudaError_t launch_rank_ids(const int32_t *topk_idx, int T, int K, int E, int R,
                             int32_t *rank_idx, cudaStream_t stream);
 cudaError_t launch_rank_expand(const ep_layout_t &rank_layout, const ep_layout_t &layout,

@@ -91,6 +91,11 @@ typedef enum ep_quant {
                               ([PR-35634] "Implementation": Blackwell packed UE8M0) */
 } ep_quant_t;
 
+typedef enum ep_route {
+    EP_ROUTE_SOFTMAX = 0,        /* softmax top-K, weights renormalised over the picks */
+    EP_ROUTE_GROUPED_SIGMOID = 1 /* sigmoid + bias, group-limited top-K (DeepSeek-V3)  */
+} ep_route_t;
+
 #define EP_MAX_TOPK 32     /* [PR-24443] review: kNumTopk <= 32 */
 #define EP_MAX_EXPERTS 1024
 #define EP_MAX_ALIGN 128
@@ -247,6 +252,33 @@ ep_status_t ep_masked_repack(const ep_layout_t *layout, const void *rows,
                              const void *row_scales, int32_t hidden, ep_quant_t quant,
                              int32_t capacity, void *slab, void *slab_scales,
                              int32_t *masked_m, ep_stream_t stream);
+
+/*
+ * ep_route_topk -- router output from logits: the topk_idx / topk_w that
+ * ep_layout and ep_combine take ([PR-24443] "Motivation": V2 dispatch infers
+ * its layout from topk_idx), for the router families of the models
+ * [PR-35634] "Supported scope" lists (Qwen3-MoE softmax, DeepSeek-V3/V4
+ * grouped sigmoid).
+ *
+ *   logits     device fp32 [T, E], finite.
+ *   bias       device fp32 [E] added to the sigmoid scores (grouped mode), or
+ *              NULL for none; ignored in softmax mode.
+ *   mode       EP_ROUTE_SOFTMAX: the K largest softmax probabilities (the K
+ *              largest logits), w = p / sum(p over the K).
+ *              EP_ROUTE_GROUPED_SIGMOID: s = sigmoid(logit), c = s + bias;
+ *              group score = sum of the two largest c in each of n_group
+ *              groups of E/n_group; the topk_group best groups are kept; the
+ *              K largest c among their experts; w = s / sum(s over the K).
+ *   n_group, topk_group  grouped mode: 1 <= n_group <= 32, E % n_group == 0,
+ *              E/n_group >= 2, 1 <= topk_group <= n_group,
+ *              K <= topk_group * E / n_group; ignored in softmax mode.
+ *   topk_idx   device int32 [T, K] (picks in rank order); topk_w fp32 [T, K].
+ * Ties go to the lower expert / group id; selections are decided in fp32.
+ */
+ep_status_t ep_route_topk(const float *logits, const float *bias, int32_t num_tokens,
+                          int32_t num_experts, int32_t num_topk, ep_route_t mode,
+                          int32_t n_group, int32_t topk_group, int32_t *topk_idx, float *topk_w,
+                          ep_stream_t stream);
 
 /*
  * ep_rank_layout -- per-logical-rank deduplicated send layout: a token is sent

@@ -1,0 +1,102 @@
+"""ep_route_topk on the GPU against the oracle router.
+
+Indices: softmax selection ranks the logits, so it must match exactly (exact
+ties included).  The grouped sigmoid selection ranks fp32 sigmoid scores; the
+GPU's expf and the host's expf may differ in the last place, so a token may
+differ only where the decision is a near-tie at fp32 resolution (checked in
+fp64), and such tokens must stay rare.  Weights: within 2^-16 relative of the
+oracle's fp64 weights (a handful of fp32 roundings of values in (0, 1]).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+from combine_expert_histogram_gb300 import binding as ep
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+W_TOL = 2.0 ** -16
+
+
+@pytest.mark.parametrize("T,E,K,ties", [(256, 128, 8, False), (16384, 256, 8, False),
+                                        (512, 64, 6, True), (300, 1024, 32, False),
+                                        (100, 4, 4, True)])
+def test_softmax_route(T, E, K, ties):
+    rng = np.random.default_rng(T + E)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    if ties:
+        lg = np.round(lg * 2) / 2
+    idx, w = ep.ep_route_topk(torch.from_numpy(lg).cuda(), K, "softmax")
+    torch.cuda.synchronize()
+    o_idx, o_w, _ = oracle.default().route_topk(lg, K, "softmax")
+    assert np.array_equal(idx.cpu().numpy(), o_idx)
+    g = w.cpu().numpy().astype(np.float64)
+    assert (np.abs(g - o_w) <= W_TOL * np.abs(o_w)).all()
+
+
+def _margins(lg, bias, G, TG, K):
+    """fp64 gaps at the group and the expert decision boundaries, per token."""
+    s = 1.0 / (1.0 + np.exp(-lg.astype(np.float64)))
+    c = s + bias.astype(np.float64)
+    T, E = c.shape
+    gs = E // G
+    top2 = -np.sort(-c.reshape(T, G, gs), axis=2)[:, :, :2].sum(axis=2)
+    gsorted = -np.sort(-top2, axis=1)
+    g_gap = gsorted[:, TG - 1] - gsorted[:, TG] if TG < G else np.full(T, np.inf)
+    keep = np.argsort(-top2, axis=1, kind="stable")[:, :TG]
+    mask = np.zeros((T, G), dtype=bool)
+    np.put_along_axis(mask, keep, True, axis=1)
+    cm = np.where(np.repeat(mask, gs, axis=1), c, -np.inf)
+    csorted = -np.sort(-cm, axis=1)
+    e_gap = csorted[:, K - 1] - csorted[:, K] if K < TG * gs else np.full(T, np.inf)
+    return np.minimum(g_gap, e_gap)
+
+
+@pytest.mark.parametrize("T,E,K,G,TG", [(1024, 256, 8, 8, 4), (16384, 256, 8, 8, 4),
+                                        (500, 64, 6, 4, 2), (200, 1024, 32, 32, 8)])
+def test_grouped_sigmoid_route(T, E, K, G, TG):
+    rng = np.random.default_rng(T * 7 + E)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    idx, w = ep.ep_route_topk(torch.from_numpy(lg).cuda(), K, "grouped_sigmoid",
+                              bias=torch.from_numpy(bias).cuda(), n_group=G, topk_group=TG)
+    torch.cuda.synchronize()
+    o_idx, o_w, _ = oracle.default().route_topk(lg, K, "grouped_sigmoid", bias=bias,
+                                                n_group=G, topk_group=TG)
+    gi = idx.cpu().numpy()
+    diff = np.nonzero((gi != o_idx).any(axis=1))[0]
+    if diff.size:
+        m = _margins(lg, bias, G, TG, K)
+        assert (m[diff] < 1e-5).all(), "selection differs away from an fp32 near-tie"
+        assert diff.size <= max(2, T // 1000)
+    same = np.setdiff1d(np.arange(T), diff)
+    g = w.cpu().numpy().astype(np.float64)[same]
+    assert (np.abs(g - o_w[same]) <= W_TOL * np.abs(o_w[same])).all()
+    # every pick lies in one of the kept groups, and picks are distinct
+    assert all(len(set(r)) == K for r in gi[:200])
+
+
+def test_route_then_layout_chain():
+    """Router output straight into layout, dispatch and combine (oracle on the same ids)."""
+    from tests import gpu_harness as gh
+    import workloads
+    T, E, K, H = 2048, 256, 8, 1024
+    rng = np.random.default_rng(3)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    idx_d, w_d = ep.ep_route_topk(torch.from_numpy(lg).cuda(), K, "grouped_sigmoid",
+                                  bias=torch.from_numpy(bias).cuda(), n_group=8, topk_group=4)
+    w = workloads.Workload("chain", T=T, H=H, E=E, K=K, routing="grouped_sigmoid",
+                           layout="contig", quant="fp8_f32", align=128)
+    x = workloads.make_x(w)
+    case = dict(idx=idx_d.cpu().numpy(), w=w_d.cpu().numpy(), x=x, idx_d=idx_d, w_d=w_d,
+                x_d=torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
+    g = gh.run_gpu(w, case)
+    ref = gh.check_layout(w, case, g)
+    gh.check_dispatch(w, case, g, ref)
+    assert gh.check_combine(w, case, g, ref) == 1.0
