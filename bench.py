@@ -376,10 +376,16 @@ def run_ours(args, w):
         line["clocks"] = sampler.summary(t_wall0, t_wall1)
     if e2e:
         line["e2e"] = e2e
-    if not args.skip_decode:
+    sections = set(args.sections.split(",")) if args.sections else set()
+    if args.skip_decode:
+        sections = set()
+    if "variants" in sections:
         line["dispatch_variants"] = measure_dispatch_variants(ep, w, L, x_d, dev)
+    if "decode" in sections:
         line["decode"] = measure_decode(ep, dev)
+    if "rank" in sections:
         line["rank_dedup"] = measure_rank_dedup(ep, dev)
+    if "router" in sections:
         line["router"] = measure_router(ep, dev)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, idx, wts, x)
@@ -652,7 +658,11 @@ def main():
     ap.add_argument("--event-every", type=int, default=10,
                     help="per-kernel CUDA events on every N-th timed step")
     ap.add_argument("--skip-decode", action="store_true",
-                    help="omit the decode-shape (masked layout) measurements")
+                    help="omit every extra measurement section (same as --sections '')")
+    ap.add_argument("--sections", default="variants,decode,rank,router",
+                    help="extra measurements after the timed steps: variants (dispatch in "
+                         "every quantisation mode), decode (masked decode shapes), rank "
+                         "(per-rank deduplicated sending), router (ep_route_topk)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (small cases for profiling; not a bench line)")
     args = ap.parse_args()
