@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kMaxThreads)
     // remaining scale rows: 4-byte words by the other threads (row-major, or
     // MN-major: word wd of row d at wd*stride + d, per expert for masked)
     if (Q != EP_QUANT_NONE && !bulk_scales) {
-        const int words = scale_bytes >> 2;
+        const int words = Q == EP_QUANT_NONE ? 1 : scale_bytes >> 2;  // (bf16 never gets here)
         for (int j = threadIdx.x; j < K * words; j += blockDim.x) {
             const int k = j / words, wd = j - k * words;
             const int d = sdst[k];
