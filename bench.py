@@ -149,6 +149,22 @@ class ClockSampler:
                 "samples": len(inwin), "window": window}
 
 
+def bench_config(w, world: int) -> dict:
+    """The workload description both arms print."""
+    rows = w.T * w.K + min(w.E, w.T * w.K) * (w.align - 1)
+    return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "K": w.K,
+            "routing": {"softmax": "softmax top-k, renormalised",
+                        "grouped_sigmoid": "grouped sigmoid + N(0,0.1) bias, "
+                                           f"{w.n_group} groups / top-{w.topk_group}",
+                        "zipf": "Zipf(1.2) without replacement"}[w.routing],
+            "layout": ("expert-contiguous, %d-row aligned" % w.align) if w.layout == "contig"
+                      else "masked [E, %d, H]" % w.cap,
+            "quant": w.quant,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": (f"inputs larger than L2: x {w.T * w.H * 2 / 1e6:.0f} MB, "
+                   f"y {rows * w.H * 2 / 1e9:.2f} GB (L2 129 MB); no flush")}
+
+
 # ------------------------------------------------------------ replicas
 def max_over_ranks(value: float, device=None) -> float:
     """Max of a per-rank number over the process group (identity without one)."""
@@ -224,13 +240,12 @@ def run_reference(args, w):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total_dt / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 dispatch, fp32-accumulate combine",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "K": w.K,
-                       "layout": "contig align 128", "quant": w.quant,
-                       "sample_tokens_per_step": n},
+            "config": bench_config(w, 1),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"first {n} of {w.T} tokens per step"},
+                             "sample": f"first {n} of {w.T} tokens per step, one pass of "
+                                       "layout + dispatch + combine, single-threaded C oracle"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -353,15 +368,11 @@ def run_ours(args, w):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8-e4m3 dispatch (fp32 scales), bf16 in / fp32-accumulate combine",
+        "dtype": "f32",
+        "formats": "bf16 activations in; E4M3 rows + fp32 1x128 scales out of dispatch; "
+                   "bf16 expert outputs in, fp32 accumulation, bf16 out of combine",
         "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "K": w.K,
-                   "routing": "grouped sigmoid + N(0,0.1) bias, 8 groups / top-4",
-                   "layout": "expert-contiguous, 128-row aligned", "quant": w.quant,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": (f"inputs larger than L2: x {x_d.numel() * 2 / 1e6:.0f} MB, "
-                          f"y {y.numel() * 2 / 1e9:.2f} GB, rows {out_rows.numel() / 1e9:.2f} GB "
-                          f"(L2 129 MB); no flush")},
+        "config": bench_config(w, world),
         "step_gbs": round(sum(ab.values()) * args.steps * world / (elapsed_ms * 1e-3) / 1e9, 1),
         "kernels": kern,
         "kernel_events": f"per-kernel events on {len(evs)} of {args.steps} timed steps",
