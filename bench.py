@@ -405,11 +405,49 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
-def measure_decode(ep, dev, reps=50):
-    """Decode shapes (masked layouts): per-step latency with L2 flushed before every
-    rep, CUDA-graph replay latency (warm L2), and the masked repack on its own."""
+def graph_time_us(fns, stream, reps=10, flush=None):
+    """GPU time of one pass of `fns` (callables launching on `stream`), from a
+    CUDA graph holding `reps` passes back to back: no host launch overhead
+    enters.  With `flush` (a callable writing 2x L2), each pass starts from a
+    flushed L2 and a flush-only graph's time is subtracted."""
     import torch
-    flush = torch.empty(2 * L2_BYTES // 4 * 4, dtype=torch.uint8, device=dev)  # 2x L2
+
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                body()
+        return g
+
+    def run(g):
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+    def body():
+        if flush is not None:
+            flush()
+        for f in fns:
+            f()
+
+    with torch.cuda.stream(stream):
+        t = run(capture(body))
+        if flush is not None:
+            t -= run(capture(flush))
+    return t
+
+
+def measure_decode(ep, dev, reps=10):
+    """Decode shapes (masked layouts), timed from CUDA graphs: the whole step
+    back to back (warm L2), each kernel from a flushed L2, and the masked
+    repack on its own."""
+    import torch
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)  # 2x L2
     res = {}
     for name in ("qwen3_30b_a3b_decode", "dsv3_decode"):
         w = workloads.CONFIGS[name]
@@ -420,80 +458,44 @@ def measure_decode(ep, dev, reps=50):
         L = ep.new_layout(w.T, w.K, w.E, "masked", capacity=w.cap, device=dev)
         rows = L.rows_capacity
         out_rows = torch.empty((rows, w.H), dtype=torch.uint8, device=dev)
-        sc = torch.empty((rows, ep.ep_scale_cols(w.H, w.quant)), device=dev,
-                         dtype=torch.float32 if w.quant == "fp8_f32" else torch.int32)
+        sc = ep.scale_buffer(L, w.H, w.quant, device=dev)
         y = workloads.make_expert_outputs(rows, w.H, seed=3, device=dev)
         out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
         s = torch.cuda.Stream(device=dev)
-
-        def step():
-            ep.ep_layout(idx_d, w.E, out=L, stream=s)
-            ep.ep_dispatch(L, x_d, w.quant, out_rows=out_rows, out_scales=sc, stream=s)
-            ep.ep_combine(L, y, w_d, out=out, stream=s)
-
+        lay = lambda: ep.ep_layout(idx_d, w.E, out=L, stream=s)
+        dis = lambda: ep.ep_dispatch(L, x_d, w.quant, out_rows=out_rows, out_scales=sc, stream=s)
+        com = lambda: ep.ep_combine(L, y, w_d, out=out, stream=s)
+        flush = lambda: flush_buf.fill_(1)
         with torch.cuda.stream(s):
             for _ in range(3):
-                step()
+                lay(), dis(), com()
         torch.cuda.synchronize()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
-        with torch.cuda.stream(s):
-            for i in range(reps):
-                flush.fill_(i & 0xFF)
-                ev[i][0].record(s)
-                ep.ep_layout(idx_d, w.E, out=L, stream=s)
-                ev[i][1].record(s)
-                ep.ep_dispatch(L, x_d, w.quant, out_rows=out_rows, out_scales=sc, stream=s)
-                ev[i][2].record(s)
-                ep.ep_combine(L, y, w_d, out=out, stream=s)
-                ev[i][3].record(s)
-        torch.cuda.synchronize()
-        seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
-                        for e in ev]) * 1e3
-        med = np.median(seg, axis=0)
+        step_us = graph_time_us([lay, dis, com], s, reps)
+        cold = {k: graph_time_us([f], s, reps, flush=flush)
+                for k, f in (("layout", lay), ("dispatch", dis), ("combine", com))}
         ab = algorithmic_bytes(w)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            step()
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        graph_us = a.elapsed_time(b) * 1e3 / reps
-        # masked repack from a contiguous layout (same routing), L2 flushed
+        # masked repack from a contiguous layout (same routing)
         Lc = ep.new_layout(w.T, w.K, w.E, "contig", align=128, device=dev)
         ep.ep_layout(idx_d, w.E, out=Lc)
-        rc = Lc.rows_capacity
-        rows_c = torch.empty((rc, w.H), dtype=torch.uint8, device=dev)
-        sc_c = torch.empty((rc, sc.shape[1]), dtype=sc.dtype, device=dev)
-        ep.ep_dispatch(Lc, x_d, w.quant, out_rows=rows_c, out_scales=sc_c)
+        rows_c, sc_c, _ = ep.ep_dispatch(Lc, x_d, w.quant)
         slab = torch.empty_like(out_rows)
         slab_sc = torch.empty_like(sc)
         mm = torch.empty(w.E, dtype=torch.int32, device=dev)
-        rts = []
-        for i in range(reps):
-            flush.fill_(i & 0xFF)
-            a.record()
-            ep.ep_masked_repack(Lc, rows_c, sc_c, w.quant, w.cap, slab=slab, slab_scales=slab_sc,
-                                masked_m=mm)
-            b.record()
-            torch.cuda.synchronize()
-            rts.append(a.elapsed_time(b) * 1e3)
-        rep_us = float(np.median(rts))
-        rep_bytes = 2 * w.T * w.K * (w.H + 4 * sc.shape[1])  # valid rows read + written
+        rep = lambda: ep.ep_masked_repack(Lc, rows_c, sc_c, w.quant, w.cap, slab=slab,
+                                          slab_scales=slab_sc, masked_m=mm, stream=s)
+        with torch.cuda.stream(s):
+            rep()
+        torch.cuda.synchronize()
+        rep_us = graph_time_us([rep], s, reps, flush=flush)
+        rep_bytes = 2 * w.T * w.K * (w.H + 4 * sc.shape[-1])  # valid rows read + written
         res[name] = {
             "T": w.T, "H": w.H, "E": w.E, "K": w.K, "cap": w.cap, "quant": w.quant,
-            "l2_flushed_us": {"layout": round(med[0], 2), "dispatch": round(med[1], 2),
-                              "combine": round(med[2], 2), "step": round(float(med.sum()), 2)},
-            "dispatch_GBps": round(ab["dispatch"] / (med[1] * 1e-6) / 1e9, 1),
-            "combine_GBps": round(ab["combine"] / (med[2] * 1e-6) / 1e9, 1),
-            "tokens_per_s_flushed": round(w.T / (med.sum() * 1e-6), 1),
-            "graph_replay_us_warm_l2": round(graph_us, 2),
-            "masked_repack_us": round(rep_us, 2),
+            "step_us_graph": round(step_us, 2),
+            "tokens_per_s": round(w.T / (step_us * 1e-6), 1),
+            "l2_flushed_us": {k: round(v, 2) for k, v in cold.items()},
+            "dispatch_GBps_flushed": round(ab["dispatch"] / (cold["dispatch"] * 1e-6) / 1e9, 1),
+            "combine_GBps_flushed": round(ab["combine"] / (cold["combine"] * 1e-6) / 1e9, 1),
+            "masked_repack_us_flushed": round(rep_us, 2),
             "masked_repack_GBps": round(rep_bytes / (rep_us * 1e-6) / 1e9, 1),
         }
         del y, out_rows, slab, rows_c
@@ -528,7 +530,8 @@ def measure_dispatch_variants(ep, w, L, x_d, dev, reps=20):
 
 
 def measure_router(ep, dev, reps=20):
-    """ep_route_topk at the two router families' bench shapes (fp32 logits)."""
+    """ep_route_topk at the two router families' bench shapes (fp32 logits),
+    timed from a CUDA graph of back-to-back calls."""
     import torch
     res = {}
     for name, T, E, K, mode, G, TG in (("dsv3_prefill", 16384, 256, 8, "grouped_sigmoid", 8, 4),
@@ -540,20 +543,17 @@ def measure_router(ep, dev, reps=20):
         bias = torch.randn(E, generator=g, device=dev, dtype=torch.float32) * 0.1
         idx = torch.empty((T, K), dtype=torch.int32, device=dev)
         wts = torch.empty((T, K), dtype=torch.float32, device=dev)
+        s = torch.cuda.Stream(device=dev)
 
         def run():
             ep.ep_route_topk(lg, K, mode, bias=bias, n_group=G, topk_group=TG, topk_idx=idx,
-                             topk_w=wts)
+                             topk_w=wts, stream=s)
 
-        for _ in range(3):
-            run()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            run()
-        b.record()
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                run()
         torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / reps
+        us = graph_time_us([run], s, reps)
         nbytes = T * E * 4 + E * 4 + T * K * 8
         res[name] = {"mode": mode, "T": T, "E": E, "K": K, "us": round(us, 2),
                      "tokens_per_s": round(T / (us * 1e-6), 1),
@@ -561,10 +561,10 @@ def measure_router(ep, dev, reps=20):
     return res
 
 
-def measure_rank_dedup(ep, dev, reps=20):
+def measure_rank_dedup(ep, dev, reps=10):
     """Per-rank deduplicated sending at the Zipf workload (8 logical ranks):
     rank layout + dispatch into the send buffer + local expand, beside the
-    direct dispatch of the same tokens."""
+    direct dispatch of the same tokens (CUDA-graph timing)."""
     import torch
     w = workloads.CONFIGS["skewed_zipf"]
     idx, wts, x = workloads.make_inputs(w)
@@ -578,22 +578,20 @@ def measure_rank_dedup(ep, dev, reps=20):
     torch.cuda.synchronize()
     send_n = int(RL.expert_offset[-1].item())
 
-    def timed(fn):
-        for _ in range(3):
-            fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            fn()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) * 1e3 / reps
+    s = torch.cuda.Stream(device=dev)
 
-    t_rl = timed(lambda: ep.ep_rank_layout(idx_d, w.E, w.R, out=RL, rank_idx=rank_idx))
-    t_send = timed(lambda: ep.ep_dispatch(RL, x_d, w.quant, out_rows=send_rows))
+    def timed(fn):
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize()
+        return graph_time_us([fn], s, reps)
+
+    t_rl = timed(lambda: ep.ep_rank_layout(idx_d, w.E, w.R, out=RL, rank_idx=rank_idx, stream=s))
+    t_send = timed(lambda: ep.ep_dispatch(RL, x_d, w.quant, out_rows=send_rows, stream=s))
     t_exp = timed(lambda: ep.ep_rank_expand(RL, L, idx_d, w.quant, send_rows, None,
-                                            out_rows=out_rows))
-    t_direct = timed(lambda: ep.ep_dispatch(L, x_d, w.quant, out_rows=direct))
+                                            out_rows=out_rows, stream=s))
+    t_direct = timed(lambda: ep.ep_dispatch(L, x_d, w.quant, out_rows=direct, stream=s))
     row = 2 * w.H
     send_bytes = w.T * row + send_n * row + w.T * w.K * 4
     exp_bytes = send_n * row + w.T * w.K * row + 2 * w.T * w.K * 4

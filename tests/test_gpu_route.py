@@ -25,7 +25,8 @@ W_TOL = 2.0 ** -16
 
 @pytest.mark.parametrize("T,E,K,ties", [(256, 128, 8, False), (16384, 256, 8, False),
                                         (512, 64, 6, True), (300, 1024, 32, False),
-                                        (100, 4, 4, True)])
+                                        (100, 4, 4, True), (200, 32, 3, True),
+                                        (150, 40, 7, True), (100, 1000, 8, False)])
 def test_softmax_route(T, E, K, ties):
     rng = np.random.default_rng(T + E)
     lg = rng.standard_normal((T, E)).astype(np.float32)
@@ -58,7 +59,10 @@ def _margins(lg, bias, G, TG, K):
 
 
 @pytest.mark.parametrize("T,E,K,G,TG", [(1024, 256, 8, 8, 4), (16384, 256, 8, 8, 4),
-                                        (500, 64, 6, 4, 2), (200, 1024, 32, 32, 8)])
+                                        (500, 64, 6, 4, 2), (200, 1024, 32, 32, 8),
+                                        (300, 32, 4, 16, 4), (400, 128, 8, 1, 1),
+                                        # shapes outside the register path (shared memory)
+                                        (300, 96, 6, 4, 2), (250, 48, 5, 3, 2)])
 def test_grouped_sigmoid_route(T, E, K, G, TG):
     rng = np.random.default_rng(T * 7 + E)
     lg = rng.standard_normal((T, E)).astype(np.float32)
