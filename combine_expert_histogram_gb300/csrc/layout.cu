@@ -14,12 +14,14 @@
 //   * lanes holding the same expert in a round find each other with
 //     ceil(log2(E+1)) independent __ballot_sync's (one per bit of the id);
 //     the mask is kept per round and reused for ranking;
-//   * up to 8192 entries (decode batches) one 1024-thread CTA does everything
-//     in one kernel; above that, tiles of 2048 entries on 256-thread CTAs:
-//     tile_hist_kernel writes each tile's expert histogram to the scratch
-//     workspace [tiles][E], then assign_kernel (launched as a programmatic
-//     dependent, so its loads and ballots overlap tile_hist) waits for it and
-//     sums the workspace columns into the expert totals and its tile's base;
+//   * up to 1024 entries one 1024-thread CTA does everything in one kernel;
+//     above that, tiles of 1024 entries (2048 beyond 32768) on 256-thread
+//     CTAs, so that the ballot work of decode-sized batches spreads over SMs:
+//     tile_hist_kernel counts each tile's experts (shared-memory atomics;
+//     counts need no order) into the scratch workspace [tiles][E], then
+//     assign_kernel (launched as a programmatic dependent, so its loads and
+//     ballots overlap tile_hist) waits for it and sums the workspace columns
+//     into the expert totals and its tile's base;
 //   * assign_kernel scans the padded counts, turns per-warp histograms into
 //     per-warp starting slots and gives each entry
 //     slot = warp base + #lower lanes with the same expert: exactly ascending
@@ -37,8 +39,7 @@ constexpr int kFillCtas = 128;
 constexpr int kSumChunk = 16;    // workspace loads in flight per thread
 constexpr int kSmallThreads = 1024;                     // single-tile CTA
 constexpr int kTileThreads = 256;                       // multi-tile CTAs
-constexpr int kSmallMax = kSmallThreads / 32 * kChunk;  // 8192 entries
-constexpr int kTile = kTileThreads / 32 * kChunk;       // 2048 entries
+constexpr int kSmallMax = kSmallThreads;                // 1024 entries: one round per warp
 
 __host__ __device__ inline int round_up_pow2(int v, int a) { return (v + a - 1) & ~(a - 1); }
 
@@ -95,21 +96,13 @@ __global__ void __launch_bounds__(kTileThreads)
     pdl_launch_dependents();  // the assign kernel may start its own loads now
     extern __shared__ int32_t hist[];  // [E]
     for (int e = threadIdx.x; e < E; e += kTileThreads) hist[e] = 0;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+    // counts only: order does not matter, one shared-memory atomic per entry
     const int start = blockIdx.x * tile;
     const int end = min(TK, start + tile);
-    Chunk c;
-    __syncthreads();  // hist zeroed
-    // tiles larger than kTile (huge inputs) are walked in kTile-sized passes
-    for (int base = start; base < end; base += kTile) {  // block-uniform
-        const int c0 = base + warp * kChunk;
-        const int c1 = min(end, c0 + kChunk);
-        load_chunk(idx, c0, c1, E, id_bits(E), c);
-#pragma unroll
-        for (int r = 0; r < kRounds; ++r) {
-            const int e = c.ev[r];
-            if (e < E && lane == __ffs(c.peers[r]) - 1) atomicAdd(&hist[e], __popc(c.peers[r]));
-        }
+    for (int i = start + (int)threadIdx.x; i < end; i += kTileThreads) {
+        const int e = __ldg(idx + i);
+        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kTileThreads) ws[(size_t)blockIdx.x * E + e] = hist[e];
@@ -136,7 +129,6 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
     int32_t *wh = sm;                         // [passes][kWarps][E]: per-warp counts, then slot bases
     int32_t *tot = wh + passes * kWarps * E;  // [E] expert histogram
     int32_t *off = tot + E;                   // [E+1] first row of each expert
-    int32_t *cum = off + E + 1;               // [E+1] unpadded prefix (rank_rows)
     __shared__ int32_t scan_tmp[kWarps];
 
     pdl_launch_dependents();  // dispatch may start loading and quantising x now
@@ -168,8 +160,8 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
             }
         }
         __syncthreads();
-        for (int e = blockIdx.x; e < E; e += gridDim.x)
-            for (int r = e * a.cap + min(tot[e], a.cap) + (int)threadIdx.x; r < (e + 1) * a.cap; r += NT)
+        for (int e = blockIdx.x + (int)gridDim.x * warp; e < E; e += (int)gridDim.x * kWarps)
+            for (int r = e * a.cap + min(tot[e], a.cap) + lane; r < (e + 1) * a.cap; r += 32)
                 a.row_src[r] = -1;
         return;
     }
@@ -236,17 +228,20 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
         E, [&](int e) { return masked ? cap : round_up_pow2(tot[e], align); }, off, scan_tmp);
 
     if (blockIdx.x == 0) {
-        if (a.rank_rows)  // rows of rank r = unpadded prefix difference over its experts
-            block_exclusive_scan<NT>(E, [&](int e) { return tot[e]; }, cum, scan_tmp);
         for (int e = threadIdx.x; e < E; e += NT) {
             a.count[e] = tot[e];
             a.offset[e] = off[e];
         }
         if (threadIdx.x == 0) a.offset[E] = off[E];
-        if (a.rank_rows) {
+        if (a.rank_rows) {  // one warp per rank: sum of its experts' counts
             const int per = E / a.R;
-            for (int r = threadIdx.x; r < a.R; r += NT)
-                a.rank_rows[r] = cum[(r + 1) * per] - cum[r * per];
+            for (int r = warp; r < a.R; r += kWarps) {
+                int sum = 0;
+                for (int e = r * per + lane; e < (r + 1) * per; e += 32) sum += tot[e];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFullMask, sum, o);
+                if (lane == 0) a.rank_rows[r] = sum;
+            }
         }
     }
 
@@ -287,11 +282,11 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
 
     // 5. row_src = -1 on padding rows (contiguous) and empty slots (masked);
     //    fill CTAs, when present, took the other experts
-    if (a.row_src) {
-        for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    if (a.row_src) {  // one warp per expert
+        for (int e = blockIdx.x + (int)gridDim.x * warp; e < E; e += (int)gridDim.x * kWarps) {
             const int r0 = off[e] + (masked ? min(tot[e], cap) : tot[e]);
             const int r1 = masked ? off[e] + cap : off[e + 1];
-            for (int r = r0 + (int)threadIdx.x; r < r1; r += NT) a.row_src[r] = -1;
+            for (int r = r0 + lane; r < r1; r += 32) a.row_src[r] = -1;
         }
     }
 }
@@ -303,36 +298,36 @@ LayoutPlan layout_plan(const ep_layout_t &L) {
     const long long TK = (long long)L.num_tokens * L.num_topk;
     int warps;
     if (TK <= kSmallMax) {
-        // one 1024-thread CTA; chunks as short as possible so all warps share the work
+        // one 1024-thread CTA, one 32-entry round per warp
         p.threads = kSmallThreads;
         warps = kSmallThreads / 32;
         p.tiles = 1;
         p.passes = 1;
-        const long long per_warp = (TK + warps - 1) / warps;
-        p.chunk = (int)((per_warp + 31) / 32 * 32);
-        if (p.chunk == 0) p.chunk = 32;
+        p.chunk = 32;
         p.tile = p.chunk * warps;
     } else {
-        // tiles of kTile entries; beyond 128 tiles the tile grows in whole
-        // kTile passes instead, which bounds the workspace and the column sums
+        // 256-thread tiles: 4 rounds per warp (1024 entries) spread mid-size
+        // inputs over more SMs, 8 rounds (2048) for large ones; beyond 128
+        // tiles the tile grows in whole passes, which bounds the workspace
         p.threads = kTileThreads;
         warps = kTileThreads / 32;
-        p.chunk = kChunk;
-        long long tiles = (TK + kTile - 1) / kTile;
+        p.chunk = TK <= 32768 ? kChunk / 2 : kChunk;
+        const long long pass_len = (long long)warps * p.chunk;
+        long long tiles = (TK + pass_len - 1) / pass_len;
         p.passes = 1;
         if (tiles > 128) {
             p.passes = (int)((tiles + 127) / 128);
-            tiles = (TK + (long long)kTile * p.passes - 1) / ((long long)kTile * p.passes);
+            tiles = (TK + pass_len * p.passes - 1) / (pass_len * p.passes);
         }
         p.tiles = (int)tiles;
-        p.tile = kTile * p.passes;
+        p.tile = (int)pass_len * p.passes;
     }
     const bool fill = L.kind == EP_LAYOUT_MASKED && L.row_src != nullptr;
     p.grid = p.tiles;
     if (fill && p.grid < kFillCtas) p.grid = L.num_experts < kFillCtas ? L.num_experts : kFillCtas;
     if (p.grid < p.tiles) p.grid = p.tiles;
     p.smem = sizeof(int32_t) *
-             ((size_t)p.passes * warps * L.num_experts + 3 * (size_t)L.num_experts + 2);
+             ((size_t)p.passes * warps * L.num_experts + 2 * (size_t)L.num_experts + 1);
     p.ws_bytes = p.tiles > 1 ? sizeof(int32_t) * (size_t)p.tiles * L.num_experts : 0;
     return p;
 }

@@ -61,10 +61,11 @@ def test_sizing_helpers(lib):
     assert lib.ep_scale_cols(384, 2) == 1
     assert lib.ep_scale_cols(2048, 0) == 0
     assert lib.ep_scale_cols(200, 1) == -1
-    # up to 8192 entries one CTA, no scratch; beyond, 2048-entry tiles need tiles x E int32
-    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=1024))) == 0
+    # up to 1024 entries one CTA, no scratch; beyond, tiles of 1024 entries (2048 above
+    # 32768 entries) need tiles x E int32
+    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=128))) == 0
+    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=1025))) == 9 * 256 * 4
     assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=16384))) == 64 * 256 * 4
-    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=1025))) == 5 * 256 * 4
 
 
 def test_host_validation_returns_before_any_launch(lib):
