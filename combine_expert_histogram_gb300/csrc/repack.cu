@@ -6,7 +6,8 @@
 // Byte copy, HBM-bound.  Every CTA scans m_e = min(count[e], cap) into shared
 // memory, then its warps walk the flat list of valid rows grid-stride; a
 // binary search over the prefix finds (expert, slot) of a flat row.  One warp
-// copies one row with 16-byte vectors and its scale words with 4-byte words.
+// copies one row with 16-byte vectors (four loads in flight per lane) and its
+// scale words with 4-byte words.
 #include "ep_common.cuh"
 
 namespace ep {
@@ -50,7 +51,20 @@ __global__ void __launch_bounds__(kThreads)
         const size_t dst = (size_t)lo * cap + s;
         const uint8_t *sp = rows + src * row_bytes;
         uint8_t *dp = slab + dst * row_bytes;
-        for (int b = lane * 16; b < row_bytes; b += 32 * 16) st_v4(dp + b, ld_stream(sp + b));
+        // four 16-byte loads in flight per lane before their stores
+        for (int b0 = lane * 16; b0 < row_bytes; b0 += 4 * 32 * 16) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * 32 * 16;
+                v[u] = b < row_bytes ? ld_stream(sp + b) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * 32 * 16;
+                if (b < row_bytes) st_v4(dp + b, v[u]);
+            }
+        }
         if (scale_bytes && mn_src_stride) {
             const uint32_t *ss = reinterpret_cast<const uint32_t *>(row_scales);
             uint32_t *ds = reinterpret_cast<uint32_t *>(slab_scales);
