@@ -18,7 +18,8 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libep.so")
 
-EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CAPACITY, EP_ERR_BAD_EXPERT_ID, EP_ERR_CUDA, EP_ERR_UNSUPPORTED = range(6)
+(EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CAPACITY, EP_ERR_BAD_EXPERT_ID, EP_ERR_CUDA, EP_ERR_UNSUPPORTED,
+ EP_ERR_TIMEOUT) = range(7)
 LAYOUT_KIND = {"contig": 0, "masked": 1}
 QUANT = {"none": 0, "fp8_f32": 1, "fp8_ue8m0": 2, "mxfp8": 3, "fp8_ue8m0_mn": 4}
 MAX_TOPK, MAX_EXPERTS, MAX_ALIGN = 32, 1024, 128

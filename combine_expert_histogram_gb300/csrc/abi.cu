@@ -66,7 +66,7 @@ ep_status_t check_layout(const ep_layout_t *L) {
 }
 
 ep_status_t check_hidden(int32_t H, ep_quant_t quant) {
-    if (H <= 0) return EP_ERR_INVALID_ARG;
+    if (H <= 0 || H > EP_MAX_HIDDEN) return EP_ERR_INVALID_ARG;
     if (quant == EP_QUANT_NONE) return H % 8 == 0 ? EP_OK : EP_ERR_INVALID_ARG;
     if (quant == EP_QUANT_FP8_F32 || quant == EP_QUANT_FP8_UE8M0 || quant == EP_QUANT_MXFP8 ||
         quant == EP_QUANT_FP8_UE8M0_MN)
@@ -91,6 +91,7 @@ const char *ep_status_str(ep_status_t s) {
         case EP_ERR_BAD_EXPERT_ID: return "EP_ERR_BAD_EXPERT_ID: expert id outside [-1, num_experts)";
         case EP_ERR_CUDA: return "EP_ERR_CUDA: a CUDA launch failed";
         case EP_ERR_UNSUPPORTED: return "EP_ERR_UNSUPPORTED";
+        case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT: a device-side copy did not complete in time";
     }
     return "unknown ep_status_t";
 }

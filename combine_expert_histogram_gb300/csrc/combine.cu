@@ -22,9 +22,8 @@ constexpr int kThreads = 256;
 constexpr int kBatch = 8;
 
 __global__ void __launch_bounds__(kThreads)
-    combine_kernel(const uint16_t *__restrict__ y, int K, int H, long long n_chunks,
-                   const int32_t *__restrict__ dst_row, const float *__restrict__ topk_w,
-                   uint16_t *__restrict__ out) {
+    combine_kernel(const uint16_t *y, int K, int H, long long n_chunks, const int32_t *dst_row,
+                   const float *topk_w, uint16_t *__restrict__ out) {
     // Launched as a programmatic dependent: wait for the previous kernel on
     // the stream (it may have produced y) before reading anything.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -47,12 +46,12 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int k = k0 + u;
-            d[u] = k < K ? __ldg(drow + k) : -1;
-            w[u] = k < K ? __ldg(wrow + k) : 0.0f;
+            d[u] = k < K ? ld_dep(drow + k) : -1;
+            w[u] = k < K ? ld_dep(wrow + k) : 0.0f;
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
-            v[u] = d[u] >= 0 ? ld_stream(y + (size_t)d[u] * H + j * 8) : make_uint4(0, 0, 0, 0);
+            v[u] = d[u] >= 0 ? ld_dep_stream(y + (size_t)d[u] * H + j * 8) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             if (d[u] < 0) continue;

@@ -10,22 +10,28 @@
 // v1.0 rule X = 2^(floor(log2 amax) - 8).
 //
 // HBM-bound: each token row is read once and written K times (80 % of the
-// bytes are writes).  One CTA owns one token:
-//   1. its threads load the row (16 bf16 = two 16-byte loads per thread),
-//      8 consecutive lanes per 128-element group; the group amax is reduced
-//      with three xor-shuffles inside those 8 lanes;
-//   2. each thread converts its 16 values to E4M3 and writes them, with the
-//      group's scale, into a shared-memory copy of the output row;
-//   3. after a proxy fence, a wait for the layout kernels (dispatch is
-//      launched as their programmatic dependent, so steps 1-2 overlap them)
-//      and a barrier, one thread issues one
-//      cp.async.bulk store per destination row (the whole H-byte row, and the
-//      fp32 scale row when its size is a multiple of 16 bytes), so the TMA
-//      engine writes K contiguous rows while the SM moves on;
-//   4. the thread waits for the bulk stores to finish reading shared memory
-//      before the CTA exits.
-// Scale rows that are not a multiple of 16 bytes (packed UE8M0, or fp32 with
-// H/128 not a multiple of 4) are written by plain 4-byte stores.
+// bytes are writes).  Persistent CTAs take tokens c, c + gridDim.x, ...; the
+// rows move through shared memory by TMA bulk copies:
+//   - a producer warp keeps a ring of `stages` x rows in flight (one
+//     cp.async.bulk global -> shared copy per row, completing on the stage's
+//     mbarrier), and hands every finished output row to the TMA engine with
+//     one bulk store per destination;
+//   - FP8: consumer warps take 16 consecutive elements per lane from the x
+//     stage (8 lanes per 1x128 group, amax by three xor-shuffles), write the
+//     E4M3 bytes into one of kOutBufs output rows and store the scale words
+//     directly from registers (gathered by shuffles); full / empty mbarrier
+//     pairs pass x stages and output rows between the two roles, so the
+//     quantisation of one token overlaps the bulk stores of the ones before;
+//   - bf16 rows need no conversion: one warp stores them straight from the
+//     x stage.
+// With few tokens per SM (decode) the ring only adds latency: there each warp
+// owns 32 slots of a row in registers and stores its 16 bytes per lane to the
+// K destinations itself (no shared memory, no barriers), the next token's
+// slots and destinations in flight meanwhile.
+// Dispatch is launched as the layout's programmatic dependent: the first rows
+// load while the layout finishes, and destinations are read only after
+// griddepcontrol.wait.  Every mbarrier wait is bounded (about a second); on
+// expiry the kernel raises EP_ERR_TIMEOUT, lets its copies land and returns.
 #include <cuda_fp8.h>
 
 #include "ep_common.cuh"
@@ -33,7 +39,13 @@
 namespace ep {
 namespace {
 
-constexpr int kMaxThreads = 512;
+constexpr int kMaxConsumerWarps = 16;
+constexpr int kMaxStages = 8;
+constexpr int kStageBudget = 144 * 1024;  // shared memory per CTA aimed for
+constexpr int kOutBufs = 4;               // FP8 output rows per CTA, at most
+constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory per CTA
+constexpr long long kWaitLimit = 1LL << 31;  // SM clocks, about a second
+constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d) {
     // __nv_cvt_float2_to_fp8x2: round to nearest even, saturate to +-448;
@@ -55,176 +67,574 @@ __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups are still reading their source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 // Make this thread's generic-proxy shared-memory writes visible to the TMA (async proxy).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Make barrier initialisation visible to the other threads and to the TMA.
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+}
+// Start the row copy global -> shared: arrive on the barrier, announcing
+// `bytes` of transactions, and issue one bulk copy that completes them.
+__device__ __forceinline__ void load_row(void *sdst, const void *gsrc, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+// Bounded wait for the phase of parity `parity` of a barrier (the phase
+// before the current one counts as complete): false once `limit` SM clocks
+// have passed, or as soon as *fail is set (when given).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *fail,
+                                          long long limit = kWaitLimit) {
+    const uint32_t a = smem_addr(bar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((fail && *fail) || clock64() - t0 > limit) return false;
+    }
+}
+
+// Quantise one FP8 slot (16 consecutive elements a, b of group j/8, part
+// lane%8 of its 8 lanes).  Returns the 16 E4M3 bytes; `sc` receives the
+// group's fp32 scale bits (FP8_F32), its UE8M0 exponent byte (FP8_UE8M0*), or
+// the E8M0 byte of the slot's 32-element block (MXFP8, shared by a lane pair).
+// Every lane of the warp must call it (shuffles over the whole warp).
 template <int Q>
-__global__ void __launch_bounds__(kMaxThreads)
-    dispatch_kernel(const uint16_t *__restrict__ x, int K, int H,
-                    const int32_t *__restrict__ dst_row, uint8_t *__restrict__ out,
-                    void *__restrict__ scales, const float *__restrict__ topk_w,
-                    float *__restrict__ row_w, bool bulk_scales, int mn_stride, int mn_cap) {
-    // bulk_scales: fp32 scale rows are a multiple of 16 bytes and `scales` is
-    // 16-byte aligned, so they go out with the TMA too
-    extern __shared__ __align__(128) uint8_t stage[];
-    const int t = blockIdx.x;
-    const int lane = threadIdx.x & 31;
-    const int G = H >> 7;
-    // staged bytes: the row (H fp8 or 2H bf16), then the scale row
-    const int row_bytes = Q == EP_QUANT_NONE ? 2 * H : H;
-    const int P4 = ((G + 3) >> 2) * 4;  // UE8M0 scale bytes per row
-    constexpr bool kUe8m0 = Q == EP_QUANT_FP8_UE8M0 || Q == EP_QUANT_FP8_UE8M0_MN;
-    const int scale_bytes = (Q == EP_QUANT_FP8_F32 || Q == EP_QUANT_MXFP8) ? 4 * G
-                            : kUe8m0 ? P4 : 0;
-    uint8_t *srow = stage;
-    uint8_t *sscale = stage + row_bytes;
-    __shared__ int32_t sdst[EP_MAX_TOPK];
-
-    if (kUe8m0 && threadIdx.x < P4 - G) sscale[G + threadIdx.x] = 127;  // 2^0
-
-    const uint16_t *xr = x + (size_t)t * H;
-    if (Q == EP_QUANT_NONE) {
-        for (int j = threadIdx.x; j < H / 8; j += blockDim.x)
-            reinterpret_cast<uint4 *>(srow)[j] = ld_stream(xr + j * 8);
+__device__ __forceinline__ uint4 quant_slot(uint4 a, uint4 b, int lane, uint32_t &sc) {
+    const unsigned gmask = 0xffu << (lane & 24);
+    float v[16];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_lo(w[i]);
+        v[2 * i + 1] = bf16_hi(w[i]);
+    }
+    uint4 q;
+    if (Q == EP_QUANT_MXFP8) {
+        // two lanes hold one 32-element block: X = 2^(floor(log2 amax) - 8),
+        // clamped at 2^-127; byte = log2(X) + 127; multiply by 1/X = 2^(127-byte)
+        float bmax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+        bmax = fmaxf(bmax, __shfl_xor_sync(gmask, bmax, 1));
+        const int be = (int)((__float_as_uint(bmax) >> 23) & 0xffu);  // 0: zero/subnormal
+        const int byte = be > 8 ? be - 8 : 0;
+        const float inv = __uint_as_float((uint32_t)(254 - byte) << 23);
+        q.x = fp8x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv), __fmul_rn(v[3], inv));
+        q.y = fp8x4(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv), __fmul_rn(v[6], inv), __fmul_rn(v[7], inv));
+        q.z = fp8x4(__fmul_rn(v[8], inv), __fmul_rn(v[9], inv), __fmul_rn(v[10], inv), __fmul_rn(v[11], inv));
+        q.w = fp8x4(__fmul_rn(v[12], inv), __fmul_rn(v[13], inv), __fmul_rn(v[14], inv), __fmul_rn(v[15], inv));
+        sc = (uint32_t)byte;
     } else {
-        // slot j: group j/8, elements (j%8)*16 .. +15 of that group
-        for (int j = threadIdx.x; j < G * 8; j += blockDim.x) {  // block-uniform trip count per warp
-            const int g = j >> 3, sub = j & 7;
-            const unsigned gmask = 0xffu << (lane & 24);
-            const uint4 a = ld_stream(xr + g * 128 + sub * 16);
-            const uint4 b = ld_stream(xr + g * 128 + sub * 16 + 8);
-            float v[16];
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                v[2 * i] = bf16_lo(w[i]);
-                v[2 * i + 1] = bf16_hi(w[i]);
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 4));
-            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
-            // s = max(amax, 1e-4) / 448, an IEEE round-to-nearest division.
-            const float s = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
-            uint4 q;
-            if (Q == EP_QUANT_FP8_F32) {
-                q.x = fp8x4(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s), __fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
-                q.y = fp8x4(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s), __fdiv_rn(v[6], s), __fdiv_rn(v[7], s));
-                q.z = fp8x4(__fdiv_rn(v[8], s), __fdiv_rn(v[9], s), __fdiv_rn(v[10], s), __fdiv_rn(v[11], s));
-                q.w = fp8x4(__fdiv_rn(v[12], s), __fdiv_rn(v[13], s), __fdiv_rn(v[14], s), __fdiv_rn(v[15], s));
-                if (sub == 0) reinterpret_cast<float *>(sscale)[g] = s;
-            } else if (Q == EP_QUANT_MXFP8) {
-                // two lanes hold one 32-element block: X = 2^(floor(log2 amax) - 8),
-                // clamped at 2^-127; byte = log2(X) + 127; multiply by 1/X = 2^(127-byte)
-                float bmax = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
-                bmax = fmaxf(bmax, __shfl_xor_sync(gmask, bmax, 1));
-                const int be = (int)((__float_as_uint(bmax) >> 23) & 0xffu);  // 0: zero/subnormal
-                const int byte = be > 8 ? be - 8 : 0;
-                const float inv = __uint_as_float((uint32_t)(254 - byte) << 23);
-                q.x = fp8x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv), __fmul_rn(v[3], inv));
-                q.y = fp8x4(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv), __fmul_rn(v[6], inv), __fmul_rn(v[7], inv));
-                q.z = fp8x4(__fmul_rn(v[8], inv), __fmul_rn(v[9], inv), __fmul_rn(v[10], inv), __fmul_rn(v[11], inv));
-                q.w = fp8x4(__fmul_rn(v[12], inv), __fmul_rn(v[13], inv), __fmul_rn(v[14], inv), __fmul_rn(v[15], inv));
-                if ((sub & 1) == 0) sscale[g * 4 + (sub >> 1)] = (uint8_t)byte;
-            } else {
-                // scale rounded up to a power of two 2^(e-127); multiply by 2^(127-e)
-                const uint32_t bits = __float_as_uint(s);
-                const int e = (int)((bits >> 23) & 0xffu) + ((bits & 0x7fffffu) != 0u);
-                const float inv = __uint_as_float((uint32_t)(254 - e) << 23);
-                q.x = fp8x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv), __fmul_rn(v[3], inv));
-                q.y = fp8x4(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv), __fmul_rn(v[6], inv), __fmul_rn(v[7], inv));
-                q.z = fp8x4(__fmul_rn(v[8], inv), __fmul_rn(v[9], inv), __fmul_rn(v[10], inv), __fmul_rn(v[11], inv));
-                q.w = fp8x4(__fmul_rn(v[12], inv), __fmul_rn(v[13], inv), __fmul_rn(v[14], inv), __fmul_rn(v[15], inv));
-                if (sub == 0) sscale[g] = (uint8_t)e;
-            }
-            reinterpret_cast<uint4 *>(srow)[j] = q;
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 4));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+        // s = max(amax, 1e-4) / 448, an IEEE round-to-nearest division.
+        const float s = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+        if (Q == EP_QUANT_FP8_F32) {
+            q.x = fp8x4(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s), __fdiv_rn(v[2], s), __fdiv_rn(v[3], s));
+            q.y = fp8x4(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s), __fdiv_rn(v[6], s), __fdiv_rn(v[7], s));
+            q.z = fp8x4(__fdiv_rn(v[8], s), __fdiv_rn(v[9], s), __fdiv_rn(v[10], s), __fdiv_rn(v[11], s));
+            q.w = fp8x4(__fdiv_rn(v[12], s), __fdiv_rn(v[13], s), __fdiv_rn(v[14], s), __fdiv_rn(v[15], s));
+            sc = __float_as_uint(s);
+        } else {
+            // scale rounded up to a power of two 2^(e-127); multiply by 2^(127-e)
+            const uint32_t bits = __float_as_uint(s);
+            const int e = (int)((bits >> 23) & 0xffu) + ((bits & 0x7fffffu) != 0u);
+            const float inv = __uint_as_float((uint32_t)(254 - e) << 23);
+            q.x = fp8x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv), __fmul_rn(v[3], inv));
+            q.y = fp8x4(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv), __fmul_rn(v[6], inv), __fmul_rn(v[7], inv));
+            q.z = fp8x4(__fmul_rn(v[8], inv), __fmul_rn(v[9], inv), __fmul_rn(v[10], inv), __fmul_rn(v[11], inv));
+            q.w = fp8x4(__fmul_rn(v[12], inv), __fmul_rn(v[13], inv), __fmul_rn(v[14], inv), __fmul_rn(v[15], inv));
+            sc = (uint32_t)e;
         }
     }
-    fence_proxy_async_smem();
-    // x was complete before the layout started; dst_row is the layout's
-    // output: wait for it (a no-op without a programmatic edge).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (threadIdx.x < K) sdst[threadIdx.x] = dst_row[(size_t)t * K + threadIdx.x];
+    return q;
+}
+
+// Scale words of one warp pass (first slot wbase = j - lane) for every
+// destination: lanes k < K hold destination k in `cd`; `sc` as quant_slot
+// returned it; G groups, `words` scale words per row.
+template <int Q>
+__device__ __forceinline__ void store_scales(uint32_t *scales, uint32_t sc, int j, int lane,
+                                             int slots, int cd, int K, int G, int words,
+                                             int mn_stride, int mn_cap) {
+    const int wbase = j - lane;
+    if constexpr (Q == EP_QUANT_FP8_F32) {
+        // group j/8's scale: lane sub of the group writes it for k = sub, sub+8, ...
+        for (int kb = 0; kb < K; kb += 8) {
+            const int k = kb + (lane & 7);
+            const int d = __shfl_sync(kFull, cd, k & 31);
+            if (j < slots && k < K && d >= 0) scales[(size_t)d * G + (j >> 3)] = sc;
+        }
+    } else if constexpr (Q == EP_QUANT_MXFP8) {
+        // the warp's 16 blocks make 4 words (word wi: slots 8wi .. 8wi+7, one
+        // byte per lane pair); lane 8wi + k%8 writes word wi for k
+        const int wi = lane >> 3;
+        uint32_t word = 0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) word |= __shfl_sync(kFull, sc, 8 * wi + 2 * m) << (8 * m);
+        const int g = (wbase >> 3) + wi;  // the word's index in the scale row
+        for (int kb = 0; kb < K; kb += 8) {
+            const int k = kb + (lane & 7);
+            const int d = __shfl_sync(kFull, cd, k & 31);
+            if (g < G && k < K && d >= 0) scales[(size_t)d * G + g] = word;
+        }
+    } else {
+        // UE8M0: the warp's 4 groups make one word, byte m = group wbase/8 + m
+        // (127 = 2^0 past the last group); lane k writes it for destination k
+        uint32_t word = 0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const uint32_t e = __shfl_sync(kFull, sc, 8 * m);
+            word |= ((wbase >> 3) + m < G ? e : 127u) << (8 * m);
+        }
+        const int wd = wbase >> 5;
+        if (lane < K && cd >= 0) {
+            size_t at = (size_t)cd * words + wd;
+            if (Q == EP_QUANT_FP8_UE8M0_MN)  // word wd of row d at wd*stride + d, per expert if masked
+                at = mn_cap ? ((size_t)(cd / mn_cap) * words + wd) * mn_stride + (size_t)(cd % mn_cap)
+                            : (size_t)wd * mn_stride + cd;
+            scales[at] = word;
+        }
+    }
+}
+
+// Tokens of CTA c in a persistent grid: c, c + step, ...
+__device__ __forceinline__ int cta_tokens(int T, int step) {
+    return T > (int)blockIdx.x ? (T - 1 - (int)blockIdx.x) / step + 1 : 0;
+}
+
+// FP8 dispatch: warp 0 produces (lane 0 drives the TMA), warps 1..C consume.
+// Token i of the CTA uses x stage i % stages and output row i % nob.
+template <int Q>
+__global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
+    quant_kernel(const uint16_t *__restrict__ x, int T, int K, int H, const int32_t *dst_row,
+                 uint8_t *__restrict__ out, uint32_t *__restrict__ scales, const float *topk_w,
+                 float *__restrict__ row_w, int32_t *status, int mn_stride, int mn_cap,
+                 int stages, int xstage_bytes, int nob) {
+    extern __shared__ __align__(128) uint8_t smem[];  // [stages] x rows, [nob] E4M3 rows
+    __shared__ __align__(8) uint64_t xfull[kMaxStages], xempty[kMaxStages];
+    __shared__ __align__(8) uint64_t ofull[kOutBufs], oempty[kOutBufs];
+    __shared__ int s_loads[kMaxStages];  // rows requested per stage, for the drain
+    __shared__ int s_fail;
+    constexpr bool kUe8m0 = Q == EP_QUANT_FP8_UE8M0 || Q == EP_QUANT_FP8_UE8M0_MN;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = (blockDim.x >> 5) - 1;  // consumer warps
+    const int G = H >> 7, slots = G * 8;
+    const int words = kUe8m0 ? (G + 3) >> 2 : G;
+    const uint32_t x_bytes = 2u * (uint32_t)H;
+    const int step = gridDim.x;
+    const int n = cta_tokens(T, step);
+    uint8_t *orows = smem + (size_t)stages * xstage_bytes;
+    const volatile int *fail = &s_fail;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&xfull[s], 1);
+            mbar_init(&xempty[s], C);
+            s_loads[s] = 0;
+        }
+        for (int b = 0; b < nob; ++b) {
+            mbar_init(&ofull[b], C);
+            mbar_init(&oempty[b], 1);
+        }
+        s_fail = 0;
+        mbar_init_fence();
+    }
     __syncthreads();
 
-    // one thread hands the staged row to the TMA engine, once per destination
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
+        // ---- producer: x rows in, finished rows out ----
+        if (lane == 0)
+            for (int i = 0; i < stages && i < n; ++i) {
+                load_row(smem + (size_t)i * xstage_bytes, x + (size_t)(blockIdx.x + i * step) * H,
+                         x_bytes, &xfull[i]);
+                s_loads[i] = 1;
+            }
+        // x was complete before the layout started; dst_row is the layout's
+        // output (a no-op without a programmatic edge)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        int cd = n > 0 && lane < K ? ld_dep(dst_row + (size_t)blockIdx.x * K + lane) : -1;
+        for (int i = 0; i < n; ++i) {
+            const int t = blockIdx.x + i * step;
+            const int nd = i + 1 < n && lane < K ? ld_dep(dst_row + (size_t)(t + step) * K + lane) : -1;
+            const int b = i % nob;
+            const bool ok = mbar_wait(&ofull[b], (i / nob) & 1, fail);
+            if (__any_sync(kFull, !ok)) {  // the whole warp leaves together
+                s_fail = 1;
+                break;
+            }
+            const uint8_t *orow = orows + (size_t)b * H;
+            for (int k = 0; k < K; ++k) {
+                const int d = __shfl_sync(kFull, cd, k);
+                if (lane == 0 && d >= 0) bulk_store(out + (size_t)d * H, orow, (uint32_t)H);
+            }
+            if (lane == 0) {
+                bulk_commit();
+                if (i > 0) {  // the previous row is free once its stores have read it
+                    bulk_wait_read<1>();
+                    mbar_arrive(&oempty[(i - 1) % nob]);
+                }
+            }
+            if (i + stages < n) {  // refill this token's x stage once every consumer read it
+                const int s = i % stages;
+                const bool ok2 = mbar_wait(&xempty[s], (i / stages) & 1, fail);
+                if (__any_sync(kFull, !ok2)) {
+                    s_fail = 1;
+                    break;
+                }
+                if (lane == 0) {
+                    load_row(smem + (size_t)s * xstage_bytes, x + (size_t)(t + stages * step) * H,
+                             x_bytes, &xfull[s]);
+                    ++s_loads[s];
+                }
+            }
+            cd = nd;
+        }
+        if (lane == 0) bulk_wait_read<0>();  // the rows must outlive the bulk reads
+    } else {
+        // ---- consumers: quantise x stage -> output row, scales from registers ----
+        const int w = warp - 1;
+        const bool weights = row_w != nullptr && w == 0 && lane < K;
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        int cd = n > 0 && lane < K ? ld_dep(dst_row + (size_t)blockIdx.x * K + lane) : -1;
+        float cw = n > 0 && weights ? ld_dep(topk_w + (size_t)blockIdx.x * K + lane) : 0.0f;
+        for (int i = 0; i < n; ++i) {
+            const int t = blockIdx.x + i * step;
+            int nd = -1;
+            float nw = 0.0f;
+            if (i + 1 < n && lane < K) {
+                nd = ld_dep(dst_row + (size_t)(t + step) * K + lane);
+                if (weights) nw = ld_dep(topk_w + (size_t)(t + step) * K + lane);
+            }
+            const int s = i % stages, b = i % nob;
+            const bool ok = mbar_wait(&xfull[s], (i / stages) & 1, fail) &&
+                            mbar_wait(&oempty[b], ((i / nob) & 1) ^ 1, fail);
+            if (__any_sync(kFull, !ok)) {  // the whole warp leaves together
+                s_fail = 1;
+                break;
+            }
+            const uint4 *xv = reinterpret_cast<const uint4 *>(smem + (size_t)s * xstage_bytes);
+            uint4 *orow = reinterpret_cast<uint4 *>(orows + (size_t)b * H);
+            for (int j = w * 32 + lane; j - lane < slots; j += C * 32) {  // whole warps per pass
+                uint4 a = make_uint4(0, 0, 0, 0), a2 = a;
+                if (j < slots) {
+                    a = xv[2 * j];
+                    a2 = xv[2 * j + 1];
+                }
+                uint32_t sc;
+                const uint4 q = quant_slot<Q>(a, a2, lane, sc);
+                if (j < slots) orow[j] = q;
+                store_scales<Q>(scales, sc, j, lane, slots, cd, K, G, words, mn_stride, mn_cap);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&xempty[s]);
+                mbar_arrive(&ofull[b]);
+            }
+            if (weights && cd >= 0) row_w[cd] = cw;
+            cd = nd;
+            cw = nw;
+        }
+    }
+    __syncthreads();
+    if (s_fail && threadIdx.x == 0) {
+        // every thread passed griddepcontrol.wait, so the status word is ours
+        // to raise; let each stage's last row copy land before the shared
+        // memory is released
+        raise_status(status, EP_ERR_TIMEOUT);
+        const long long t0 = clock64();
+        for (int s = 0; s < stages; ++s) {
+            const long long left = kWaitLimit - (clock64() - t0);
+            if (s_loads[s] > 0 && (left <= 0 || !mbar_wait(&xfull[s], (s_loads[s] - 1) & 1, nullptr, left)))
+                break;
+        }
+    }
+}
+
+// Few tokens per SM: CTA c takes tokens c, c + gridDim.x, ...; thread i owns
+// slots i, i + blockDim.x, ... (whole warps step through the passes, lanes
+// past the last slot idle along) and keeps them in registers.
+template <int Q>
+__global__ void __launch_bounds__(512)
+    direct_kernel(const uint16_t *__restrict__ x, int T, int K, int H, const int32_t *dst_row,
+                  uint8_t *__restrict__ out, uint32_t *__restrict__ scales, const float *topk_w,
+                  float *__restrict__ row_w, int mn_stride, int mn_cap) {
+    constexpr bool kFp8 = Q != EP_QUANT_NONE;
+    constexpr bool kUe8m0 = Q == EP_QUANT_FP8_UE8M0 || Q == EP_QUANT_FP8_UE8M0_MN;
+    const int lane = threadIdx.x & 31;
+    const int G = H >> 7;
+    const int row_bytes = kFp8 ? H : 2 * H;
+    const int slots = kFp8 ? G * 8 : H / 8;
+    const int words = kUe8m0 ? (G + 3) >> 2 : G;
+    const int step = gridDim.x;
+    const bool weights = row_w != nullptr && threadIdx.x < K;
+    const int n = cta_tokens(T, step);
+    // slot j of token tok: 16 bf16 (two 16-byte loads) for FP8, 8 for bf16
+    auto load = [&](int tok, int j, uint4 &a, uint4 &b) {
+        const uint16_t *xr = x + (size_t)tok * H;
+        if (kFp8) {
+            a = ld_stream(xr + j * 16);
+            b = ld_stream(xr + j * 16 + 8);
+        } else {
+            a = ld_stream(xr + j * 8);
+        }
+    };
+
+    uint4 ca = make_uint4(0, 0, 0, 0), cb = ca, na = ca, nb = ca;
+    const bool first_slot = (int)threadIdx.x < slots;
+    if (n > 0 && first_slot) load(blockIdx.x, threadIdx.x, ca, cb);
+    // x was complete before the layout started; dst_row is the layout's output
+    // (a no-op without a programmatic edge)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int cd = n > 0 && lane < K ? ld_dep(dst_row + (size_t)blockIdx.x * K + lane) : -1;
+    float cw = n > 0 && weights ? ld_dep(topk_w + (size_t)blockIdx.x * K + lane) : 0.0f;
+    for (int i = 0; i < n; ++i) {
+        const int t = blockIdx.x + i * step;
+        int nd = -1;
+        float nw = 0.0f;
+        if (i + 1 < n) {  // the next token, in flight meanwhile
+            if (first_slot) load(t + step, threadIdx.x, na, nb);
+            if (lane < K) {
+                nd = ld_dep(dst_row + (size_t)(t + step) * K + lane);
+                if (weights) nw = ld_dep(topk_w + (size_t)(t + step) * K + lane);
+            }
+        }
+        for (int j = threadIdx.x; j - lane < slots; j += blockDim.x) {
+            const bool act = j < slots;
+            uint4 a = ca, b = cb;
+            if (j != (int)threadIdx.x) {  // passes beyond the first: loaded here
+                a = b = make_uint4(0, 0, 0, 0);
+                if (act) load(t, j, a, b);
+            }
+            uint4 q = a;
+            uint32_t sc = 0;
+            if constexpr (kFp8) q = quant_slot<Q>(a, b, lane, sc);
+            for (int k = 0; k < K; ++k) {  // 16 bytes per lane to each destination
+                const int d = __shfl_sync(kFull, cd, k);
+                if (act && d >= 0) st_v4(out + (size_t)d * row_bytes + (size_t)j * 16, q);
+            }
+            if constexpr (kFp8)
+                store_scales<Q>(scales, sc, j, lane, slots, cd, K, G, words, mn_stride, mn_cap);
+        }
+        if (weights && cd >= 0) row_w[cd] = cw;
+        ca = na;
+        cb = nb;
+        cd = nd;
+        cw = nw;
+    }
+}
+
+// bf16 dispatch: one warp; lane 0 drives the TMA, lanes k < K hold the
+// destinations.  Token i uses stage i % stages; a stage is refilled once the
+// stores of its token have read it.
+__global__ void __launch_bounds__(32)
+    copy_kernel(const uint16_t *__restrict__ x, int T, int K, int H, const int32_t *dst_row,
+                uint8_t *__restrict__ out, const float *topk_w, float *__restrict__ row_w,
+                int32_t *status, int stages, int xstage_bytes) {
+    extern __shared__ __align__(128) uint8_t smem[];  // [stages] x rows
+    __shared__ __align__(8) uint64_t xfull[kMaxStages];
+    __shared__ int s_loads[kMaxStages];
+    const int lane = threadIdx.x;
+    const uint32_t row_bytes = 2u * (uint32_t)H;
+    const int step = gridDim.x;
+    const int n = cta_tokens(T, step);
+    const bool weights = row_w != nullptr && lane < K;
+
+    if (lane == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&xfull[s], 1);
+            s_loads[s] = s < n ? 1 : 0;
+        }
+        mbar_init_fence();
+        for (int i = 0; i < stages && i < n; ++i)
+            load_row(smem + (size_t)i * xstage_bytes, x + (size_t)(blockIdx.x + i * step) * H,
+                     row_bytes, &xfull[i]);
+    }
+    __syncwarp();
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // dst_row is the layout's output
+    int cd = n > 0 && lane < K ? ld_dep(dst_row + (size_t)blockIdx.x * K + lane) : -1;
+    float cw = n > 0 && weights ? ld_dep(topk_w + (size_t)blockIdx.x * K + lane) : 0.0f;
+    bool failed = false;
+    for (int i = 0; i < n; ++i) {
+        const int t = blockIdx.x + i * step;
+        int nd = -1;
+        float nw = 0.0f;
+        if (i + 1 < n && lane < K) {
+            nd = ld_dep(dst_row + (size_t)(t + step) * K + lane);
+            if (weights) nw = ld_dep(topk_w + (size_t)(t + step) * K + lane);
+        }
+        const int s = i % stages;
+        if (__any_sync(kFull, !mbar_wait(&xfull[s], (i / stages) & 1, nullptr))) {
+            failed = true;
+            break;
+        }
+        const uint8_t *row = smem + (size_t)s * xstage_bytes;
         for (int k = 0; k < K; ++k) {
-            const int d = sdst[k];
-            if (d < 0) continue;
-            bulk_store(out + (size_t)d * row_bytes, srow, (uint32_t)row_bytes);
-            if (bulk_scales)
-                bulk_store(static_cast<uint8_t *>(scales) + (size_t)d * scale_bytes, sscale,
-                           (uint32_t)scale_bytes);
+            const int d = __shfl_sync(kFull, cd, k);
+            if (lane == 0 && d >= 0) bulk_store(out + (size_t)d * row_bytes, row, row_bytes);
         }
-        bulk_commit();
+        if (lane == 0) {
+            bulk_commit();
+            // the previous token's stage, once its stores have read it
+            const int r = i - 1 + stages;
+            if (i > 0 && r < n) {
+                bulk_wait_read<1>();
+                const int sp = (i - 1) % stages;
+                load_row(smem + (size_t)sp * xstage_bytes, x + (size_t)(blockIdx.x + r * step) * H,
+                         row_bytes, &xfull[sp]);
+                ++s_loads[sp];
+            }
+        }
+        if (weights && cd >= 0) row_w[cd] = cw;
+        cd = nd;
+        cw = nw;
     }
-    // remaining scale rows: 4-byte words by the other threads (row-major, or
-    // MN-major: word wd of row d at wd*stride + d, per expert for masked)
-    if (Q != EP_QUANT_NONE && !bulk_scales) {
-        const int words = Q == EP_QUANT_NONE ? 1 : scale_bytes >> 2;  // (bf16 never gets here)
-        for (int j = threadIdx.x; j < K * words; j += blockDim.x) {
-            const int k = j / words, wd = j - k * words;
-            const int d = sdst[k];
-            if (d < 0) continue;
-            size_t at = (size_t)d * words + wd;
-            if (Q == EP_QUANT_FP8_UE8M0_MN)
-                at = mn_cap ? ((size_t)(d / mn_cap) * words + wd) * mn_stride + (size_t)(d % mn_cap)
-                            : (size_t)wd * mn_stride + d;
-            reinterpret_cast<uint32_t *>(scales)[at] = reinterpret_cast<const uint32_t *>(sscale)[wd];
+    if (lane == 0) {
+        bulk_wait_read<0>();
+        if (failed) {
+            raise_status(status, EP_ERR_TIMEOUT);
+            const long long t0 = clock64();
+            for (int s = 0; s < stages; ++s) {
+                const long long left = kWaitLimit - (clock64() - t0);
+                if (s_loads[s] > 0 && (left <= 0 || !mbar_wait(&xfull[s], (s_loads[s] - 1) & 1, nullptr, left)))
+                    break;
+            }
         }
     }
-    if (row_w && threadIdx.x < K) {
-        const int d = sdst[threadIdx.x];
-        if (d >= 0) row_w[d] = __ldg(topk_w + (size_t)t * K + threadIdx.x);
+}
+
+// x stages that fit the per-CTA budget beside `fixed` bytes, no more than the
+// tokens one CTA of two per SM would take, at least two.
+int stage_count(int T, int xstage_bytes, int fixed) {
+    int stages = (kStageBudget - fixed) / xstage_bytes;
+    const int per_cta = (T + 2 * sm_count() - 1) / (2 * sm_count());
+    if (stages > per_cta) stages = per_cta;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) stages = 2;
+    return stages;
+}
+
+// Persistent grid: as many CTAs as are resident at once, at most one per token.
+template <typename Kern>
+cudaError_t persistent_grid(Kern kern, int threads, size_t smem, int T, int &grid) {
+    if (smem > 48 * 1024) {
+        cudaError_t err =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
     }
-    if (threadIdx.x == 0) bulk_wait_read();  // staging must outlive the bulk reads
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (err != cudaSuccess) return err;
+    long long g = (long long)(per_sm > 0 ? per_sm : 1) * sm_count();
+    grid = (int)(g < T ? g : T);
+    return cudaSuccess;
+}
+
+// MN-major scale columns: padded row space (contiguous) or padded capacity per
+// expert (masked); returns the column stride, `cap` the capacity or 0.
+int mn_layout(const ep_layout_t &L, int &cap) {
+    const bool masked = L.kind == EP_LAYOUT_MASKED;
+    const long long TK = (long long)L.num_tokens * L.num_topk;
+    const long long rows_cap = masked ? (long long)L.num_experts * L.capacity
+                                      : TK + (TK < L.num_experts ? TK : L.num_experts) * (L.align - 1);
+    cap = masked ? L.capacity : 0;
+    return masked ? (L.capacity + 3) / 4 * 4 : (int)((rows_cap + 3) / 4 * 4);
+}
+
+// Up to this many tokens per SM the direct kernel is used.
+constexpr int kDirectTokensPerSm = 2;
+
+template <int Q>
+cudaError_t launch_direct(const ep_layout_t &L, const void *x, int H, void *out_rows,
+                          void *out_scales, const float *topk_w, float *row_w, cudaStream_t stream) {
+    const int T = L.num_tokens;
+    const int slots = Q == EP_QUANT_NONE ? H / 8 : (H / 128) * 8;
+    int threads = ((slots + 31) / 32) * 32;
+    if (threads > 512) threads = 512;
+    int grid = 0;
+    cudaError_t err = persistent_grid(direct_kernel<Q>, threads, 0, T, grid);
+    if (err != cudaSuccess) return err;
+    int mn_cap = 0;
+    const int mn_stride = mn_layout(L, mn_cap);
+    return launch_kernel(direct_kernel<Q>, grid, threads, 0, stream, true,
+                         static_cast<const uint16_t *>(x), T, L.num_topk, H, L.dst_row,
+                         static_cast<uint8_t *>(out_rows), static_cast<uint32_t *>(out_scales),
+                         topk_w, row_w, mn_stride, mn_cap);
 }
 
 template <int Q>
-cudaError_t launch_q(const ep_layout_t &L, const void *x, int H, void *out_rows,
-                     void *out_scales, const float *topk_w, float *row_w, cudaStream_t stream) {
-    const int G = H / 128;
-    const int row_bytes = Q == EP_QUANT_NONE ? 2 * H : H;
-    const int scale_bytes = (Q == EP_QUANT_FP8_F32 || Q == EP_QUANT_MXFP8) ? 4 * G
-                            : (Q == EP_QUANT_FP8_UE8M0 || Q == EP_QUANT_FP8_UE8M0_MN) ? ((G + 3) / 4) * 4
-                            : 0;
-    const size_t smem = (size_t)row_bytes + (size_t)scale_bytes;
-    // one slot per 16 elements (FP8) or per 16-byte chunk (bf16), up to 512 threads
-    int slots = Q == EP_QUANT_NONE ? H / 8 : G * 8;
-    int threads = ((slots + 31) / 32) * 32;
-    if (threads > kMaxThreads) threads = kMaxThreads;
-    if (threads < 64) threads = 64;  // K <= 32 threads read dst_row; scale pads
-    if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(dispatch_kernel<Q>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-    }
-    const bool bulk_scales = (Q == EP_QUANT_FP8_F32 || Q == EP_QUANT_MXFP8) &&
-                             (scale_bytes % 16) == 0 &&
-                             (reinterpret_cast<uintptr_t>(out_scales) % 16) == 0;
-    // programmatic dependent of the layout: x is loaded and quantised while
-    // the layout kernels finish
-    // MN-major scale columns: padded row space (contiguous) or padded capacity per expert
-    const bool masked = L.kind == EP_LAYOUT_MASKED;
-    const long long rows_cap = masked ? (long long)L.num_experts * L.capacity
-                                      : (long long)L.num_tokens * L.num_topk +
-                                            (long long)(L.num_tokens * L.num_topk < L.num_experts
-                                                            ? L.num_tokens * L.num_topk
-                                                            : L.num_experts) * (L.align - 1);
-    const int mn_cap = masked ? L.capacity : 0;
-    const int mn_stride = masked ? (L.capacity + 3) / 4 * 4 : (int)((rows_cap + 3) / 4 * 4);
-    return launch_kernel(dispatch_kernel<Q>, L.num_tokens, threads, smem, stream, true,
-                         static_cast<const uint16_t *>(x), L.num_topk, H, L.dst_row,
-                         static_cast<uint8_t *>(out_rows), out_scales, topk_w, row_w,
-                         bulk_scales, mn_stride, mn_cap);
+cudaError_t launch_quant(const ep_layout_t &L, const void *x, int H, void *out_rows,
+                         void *out_scales, const float *topk_w, float *row_w, cudaStream_t stream) {
+    const int T = L.num_tokens;
+    const int xstage_bytes = 2 * H;  // H is a multiple of 128
+    // output rows: kOutBufs, or 2 where two x stages and kOutBufs rows do not fit
+    const int nob = 2 * xstage_bytes + kOutBufs * H <= kSmemMax ? kOutBufs : 2;
+    const int stages = stage_count(T, xstage_bytes, nob * H);
+    const size_t smem = (size_t)stages * xstage_bytes + (size_t)nob * H;
+    int consumers = (H / 128 * 8 + 31) / 32;  // one slot of 16 elements per lane
+    if (consumers > kMaxConsumerWarps) consumers = kMaxConsumerWarps;
+    const int threads = 32 * (consumers + 1);
+    int grid = 0;
+    cudaError_t err = persistent_grid(quant_kernel<Q>, threads, smem, T, grid);
+    if (err != cudaSuccess) return err;
+    int mn_cap = 0;
+    const int mn_stride = mn_layout(L, mn_cap);
+    // programmatic dependent of the layout: the first rows load and quantise
+    // while the layout kernels finish
+    return launch_kernel(quant_kernel<Q>, grid, threads, smem, stream, true,
+                         static_cast<const uint16_t *>(x), T, L.num_topk, H, L.dst_row,
+                         static_cast<uint8_t *>(out_rows), static_cast<uint32_t *>(out_scales),
+                         topk_w, row_w, L.status, mn_stride, mn_cap, stages, xstage_bytes, nob);
+}
+
+cudaError_t launch_copy(const ep_layout_t &L, const void *x, int H, void *out_rows,
+                        const float *topk_w, float *row_w, cudaStream_t stream) {
+    const int T = L.num_tokens;
+    const int xstage_bytes = (2 * H + 127) / 128 * 128;
+    const int stages = stage_count(T, xstage_bytes, 0);
+    const size_t smem = (size_t)stages * xstage_bytes;
+    int grid = 0;
+    cudaError_t err = persistent_grid(copy_kernel, 32, smem, T, grid);
+    if (err != cudaSuccess) return err;
+    return launch_kernel(copy_kernel, grid, 32, smem, stream, true,
+                         static_cast<const uint16_t *>(x), T, L.num_topk, H, L.dst_row,
+                         static_cast<uint8_t *>(out_rows), topk_w, row_w, L.status, stages,
+                         xstage_bytes);
 }
 
 }  // namespace
@@ -233,17 +643,31 @@ cudaError_t launch_dispatch(const ep_layout_t &L, const void *x, int H, ep_quant
                             void *out_rows, void *out_scales, const float *topk_w,
                             float *row_w, cudaStream_t stream) {
     if (L.num_tokens == 0) return cudaSuccess;
+    if (L.num_tokens <= kDirectTokensPerSm * sm_count()) {
+        switch (quant) {
+            case EP_QUANT_NONE:
+                return launch_direct<EP_QUANT_NONE>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+            case EP_QUANT_FP8_F32:
+                return launch_direct<EP_QUANT_FP8_F32>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+            case EP_QUANT_MXFP8:
+                return launch_direct<EP_QUANT_MXFP8>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+            case EP_QUANT_FP8_UE8M0_MN:
+                return launch_direct<EP_QUANT_FP8_UE8M0_MN>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+            default:
+                return launch_direct<EP_QUANT_FP8_UE8M0>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+        }
+    }
     switch (quant) {
         case EP_QUANT_NONE:
-            return launch_q<EP_QUANT_NONE>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+            return launch_copy(L, x, H, out_rows, topk_w, row_w, stream);
         case EP_QUANT_FP8_F32:
-            return launch_q<EP_QUANT_FP8_F32>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+            return launch_quant<EP_QUANT_FP8_F32>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
         case EP_QUANT_MXFP8:
-            return launch_q<EP_QUANT_MXFP8>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+            return launch_quant<EP_QUANT_MXFP8>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
         case EP_QUANT_FP8_UE8M0_MN:
-            return launch_q<EP_QUANT_FP8_UE8M0_MN>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+            return launch_quant<EP_QUANT_FP8_UE8M0_MN>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
         default:
-            return launch_q<EP_QUANT_FP8_UE8M0>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
+            return launch_quant<EP_QUANT_FP8_UE8M0>(L, x, H, out_rows, out_scales, topk_w, row_w, stream);
     }
 }
 

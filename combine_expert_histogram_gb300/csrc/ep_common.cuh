@@ -22,12 +22,48 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-// Streaming 16-byte load of data read exactly once (no L1 allocation).
+// Streaming 16-byte load of data read exactly once (no L1 allocation), through
+// the non-coherent path: only for data that no kernel still running can write.
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
+    return v;
+}
+
+// Loads of what a programmatic predecessor wrote, issued after
+// griddepcontrol.wait.  A const __restrict__ pointer or __ldg lets the
+// compiler treat the data as read-only for the whole kernel (non-coherent
+// loads, scheduled freely), which would let the load run before the wait and
+// see the previous contents; a volatile asm load with a memory clobber stays
+// after the wait and is a coherent (weak) global load.
+__device__ __forceinline__ int32_t ld_dep(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_dep(const float *p) {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 ld_dep_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+// Streaming (no L1 allocation) form of ld_dep_v4, for rows read exactly once.
+__device__ __forceinline__ uint4 ld_dep_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
     return v;
 }
 

@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
             pdl_wait();
             for (int e = threadIdx.x; e < E; e += NT) {
                 int total = 0;
-                for (int b = 0; b < a.tiles; ++b) total += __ldcg(a.ws + (size_t)b * E + e);
+                for (int b = 0; b < a.tiles; ++b) total += ld_dep(a.ws + (size_t)b * E + e);
                 tot[e] = total;
             }
         }
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
                 int v[kSumChunk];
 #pragma unroll
                 for (int u = 0; u < kSumChunk; ++u)
-                    v[u] = b0 + u < a.tiles ? __ldcg(a.ws + (size_t)(b0 + u) * E + e) : 0;
+                    v[u] = b0 + u < a.tiles ? ld_dep(a.ws + (size_t)(b0 + u) * E + e) : 0;
 #pragma unroll
                 for (int u = 0; u < kSumChunk; ++u) {
                     base += b0 + u < tile_id ? v[u] : 0;

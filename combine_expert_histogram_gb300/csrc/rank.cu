@@ -51,10 +51,9 @@ __global__ void __launch_bounds__(kThreads)
 
 __global__ void __launch_bounds__(kThreads)
     rank_expand_kernel(const int32_t *__restrict__ idx, int K, int E, int per,
-                       const int32_t *__restrict__ send_dst, const int32_t *__restrict__ dst_row,
-                       int row_bytes, int scale_bytes, const uint8_t *__restrict__ send_rows,
-                       const uint8_t *__restrict__ send_scales, uint8_t *__restrict__ out_rows,
-                       uint8_t *__restrict__ out_scales) {
+                       const int32_t *send_dst, const int32_t *dst_row, int row_bytes,
+                       int scale_bytes, const uint8_t *send_rows, const uint8_t *send_scales,
+                       uint8_t *__restrict__ out_rows, uint8_t *__restrict__ out_scales) {
     // the send buffer is the previous kernel's output (programmatic launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int t = blockIdx.x;
@@ -62,14 +61,14 @@ __global__ void __launch_bounds__(kThreads)
     if (threadIdx.x < K) {
         const int k = threadIdx.x;
         const int e = __ldg(idx + (size_t)t * K + k);
-        const int d = dst_row[(size_t)t * K + k];
+        const int d = ld_dep(dst_row + (size_t)t * K + k);
         int src = -1;
         if (d >= 0 && e >= 0 && e < E) {
             const int r = e / per;
             for (int j = 0; j <= k; ++j) {
                 const int ej = __ldg(idx + (size_t)t * K + j);
                 if (ej >= 0 && ej < E && ej / per == r) {
-                    src = send_dst[(size_t)t * K + j];
+                    src = ld_dep(send_dst + (size_t)t * K + j);
                     break;
                 }
             }
@@ -82,7 +81,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int j = threadIdx.x; j < K * chunks; j += kThreads) {
         const int k = j / chunks, c = j - k * chunks;
         if (s_dst[k] < 0) continue;
-        const uint4 v = *reinterpret_cast<const uint4 *>(send_rows + (size_t)s_src[k] * row_bytes + 16 * c);
+        const uint4 v = ld_dep_v4(send_rows + (size_t)s_src[k] * row_bytes + 16 * c);
         st_v4(out_rows + (size_t)s_dst[k] * row_bytes + 16 * c, v);
     }
     const int words = scale_bytes >> 2;
@@ -90,7 +89,7 @@ __global__ void __launch_bounds__(kThreads)
         const int k = j / words, c = j - k * words;
         if (s_dst[k] < 0) continue;
         reinterpret_cast<uint32_t *>(out_scales + (size_t)s_dst[k] * scale_bytes)[c] =
-            reinterpret_cast<const uint32_t *>(send_scales + (size_t)s_src[k] * scale_bytes)[c];
+            (uint32_t)ld_dep(reinterpret_cast<const int32_t *>(send_scales + (size_t)s_src[k] * scale_bytes) + c);
     }
 }
 

@@ -45,7 +45,9 @@
  *   - Data-dependent errors are raised on the device into the layout's status
  *     word as the maximum of the codes seen (no trap, no assert, no
  *     out-of-bounds write): EP_ERR_BAD_EXPERT_ID for an id outside [-1, E),
- *     EP_ERR_CAPACITY for a masked expert receiving more than `capacity` rows.
+ *     EP_ERR_CAPACITY for a masked expert receiving more than `capacity` rows,
+ *     EP_ERR_TIMEOUT if a bulk copy a kernel waits for never completes (the
+ *     wait is bounded; the kernel then drains its copies and returns).
  *     Read it back after the stream completes.
  *   - bf16 means IEEE binary32's upper 16 bits; FP8 means E4M3FN (OCP OFP8).
  */
@@ -67,7 +69,9 @@ typedef enum ep_status {
     EP_ERR_CAPACITY = 2,      /* too many tokens / rows for the reserved space  */
     EP_ERR_BAD_EXPERT_ID = 3, /* device-side only: id outside [-1, E)          */
     EP_ERR_CUDA = 4,          /* a CUDA launch failed                           */
-    EP_ERR_UNSUPPORTED = 5    /* valid request this build does not implement    */
+    EP_ERR_UNSUPPORTED = 5,   /* valid request this build does not implement    */
+    EP_ERR_TIMEOUT = 6        /* device-side only: a bulk copy a kernel waited
+                                 for did not complete within about a second    */
 } ep_status_t;
 
 typedef enum ep_layout_kind {
@@ -96,6 +100,7 @@ typedef enum ep_route {
     EP_ROUTE_GROUPED_SIGMOID = 1 /* sigmoid + bias, group-limited top-K (DeepSeek-V3)  */
 } ep_route_t;
 
+#define EP_MAX_HIDDEN 32768 /* largest hidden size H (shared-memory row staging) */
 #define EP_MAX_TOPK 32     /* [PR-24443] review: kNumTopk <= 32 */
 #define EP_MAX_EXPERTS 1024
 #define EP_MAX_ALIGN 128
@@ -186,7 +191,7 @@ ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *layout, void *
  * [VLLM-EP] FP8 block-quantised dispatch).
  *
  *   x           device bf16 [T, hidden], 16-byte aligned.
- *   hidden      H; a multiple of 128 for FP8, of 8 for bf16.
+ *   hidden      H in [1, EP_MAX_HIDDEN]; a multiple of 128 for FP8, of 8 for bf16.
  *   out_rows    device [rows, H]: bf16 (EP_QUANT_NONE) or E4M3 bytes; 16-byte
  *               aligned.  Only rows named by dst_row are written; padding rows
  *               and empty slots are left untouched.

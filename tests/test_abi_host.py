@@ -61,6 +61,9 @@ def test_sizing_helpers(lib):
     assert lib.ep_scale_cols(384, 2) == 1
     assert lib.ep_scale_cols(2048, 0) == 0
     assert lib.ep_scale_cols(200, 1) == -1
+    # hidden sizes up to EP_MAX_HIDDEN = 32768 (rows are staged in shared memory)
+    assert lib.ep_scale_cols(32768, 1) == 256
+    assert lib.ep_scale_cols(32768 + 128, 1) == -1
     # up to 1024 entries one CTA, no scratch; beyond, tiles of 1024 entries (2048 above
     # 32768 entries) need tiles x E int32
     assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=128))) == 0
@@ -102,7 +105,10 @@ def test_host_validation_returns_before_any_launch(lib):
                                 ctypes.c_void_p(4096), None, ctypes.c_void_p(4096), None) == INVALID
     assert lib.ep_masked_repack(ctypes.byref(L), ctypes.c_void_p(4096), None, 7168, 0, 0,
                                 ctypes.c_void_p(4096), None, ctypes.c_void_p(4096), None) == INVALID
+    assert lib.ep_dispatch(ctypes.byref(L), ctypes.c_void_p(4096), 32776, 0, ctypes.c_void_p(4096),
+                           None, None, None, None) == INVALID
     assert lib.ep_status_str(3).decode().startswith("EP_ERR_BAD_EXPERT_ID")
+    assert lib.ep_status_str(6).decode().startswith("EP_ERR_TIMEOUT")
 
 
 def test_binding_refuses_cpu_tensors(lib):

@@ -59,6 +59,17 @@ MID = [
                        layout="contig", quant="mxfp8", align=128, seed=12),
     workloads.Workload("mxfp8_dsv3", T=2000, H=7168, E=256, K=8, routing="grouped_sigmoid",
                        layout="masked", quant="mxfp8", cap=2000, seed=13),
+    # largest hidden size: two shared-memory row stages and two output rows,
+    # several slots per lane; bf16 rows of 64 KiB; and the same width through
+    # the few-tokens-per-SM kernel (T <= 2 x 152)
+    workloads.Workload("hmax_fp8", T=700, H=32768, E=16, K=4, routing="softmax",
+                       layout="contig", quant="fp8_f32", align=16, seed=14),
+    workloads.Workload("hmax_bf16", T=650, H=32768, E=16, K=4, routing="softmax",
+                       layout="masked", quant="none", cap=650, seed=15),
+    workloads.Workload("hmax_ue8m0_few", T=301, H=32768, E=16, K=4, routing="softmax",
+                       layout="masked", quant="fp8_ue8m0", cap=301, seed=17),
+    workloads.Workload("h9216_ue8m0", T=1201, H=9216, E=32, K=6, routing="softmax",
+                       layout="contig", quant="fp8_ue8m0", align=64, seed=16),
     # > 128 tiles of 2048 entries: tiles of several passes
     workloads.Workload("multipass", T=40000, H=128, E=64, K=8, routing="softmax",
                        layout="contig", quant="fp8_ue8m0", align=128, R=4, seed=10),
