@@ -329,16 +329,51 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
         // ---- consumers: quantise x stage -> output row, scales from registers ----
         const int w = warp - 1;
         const bool weights = row_w != nullptr && w == 0 && lane < K;
+        const int j0 = w * 32 + lane;
+        // x was complete before the layout started: when one pass covers the
+        // row, the first token is quantised while the layout may still run
+        // and only its scale words wait for the destinations
+        bool early = n > 0 && slots <= C * 32;
+        uint32_t sc0 = 0;
+        if (early) {
+            const bool ok = mbar_wait(&xfull[0], 0, fail);  // output row 0 starts free
+            if (__any_sync(kFull, !ok)) {
+                s_fail = 1;
+                early = false;
+            } else {
+                const uint4 *xv = reinterpret_cast<const uint4 *>(smem);
+                uint4 a = make_uint4(0, 0, 0, 0), a2 = a;
+                if (j0 < slots) {
+                    a = xv[2 * j0];
+                    a2 = xv[2 * j0 + 1];
+                }
+                const uint4 q = quant_slot<Q>(a, a2, lane, sc0);
+                if (j0 < slots) reinterpret_cast<uint4 *>(orows)[j0] = q;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&xempty[0]);
+                    mbar_arrive(&ofull[0]);
+                }
+            }
+        }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         int cd = n > 0 && lane < K ? ld_dep(dst_row + (size_t)blockIdx.x * K + lane) : -1;
         float cw = n > 0 && weights ? ld_dep(topk_w + (size_t)blockIdx.x * K + lane) : 0.0f;
-        for (int i = 0; i < n; ++i) {
+        for (int i = 0; i < n && !*fail; ++i) {
             const int t = blockIdx.x + i * step;
             int nd = -1;
             float nw = 0.0f;
             if (i + 1 < n && lane < K) {
                 nd = ld_dep(dst_row + (size_t)(t + step) * K + lane);
                 if (weights) nw = ld_dep(topk_w + (size_t)(t + step) * K + lane);
+            }
+            if (i == 0 && early) {  // quantised above: the scale words remain
+                store_scales<Q>(scales, sc0, j0, lane, slots, cd, K, G, words, mn_stride, mn_cap);
+                if (weights && cd >= 0) row_w[cd] = cw;
+                cd = nd;
+                cw = nw;
+                continue;
             }
             const int s = i % stages, b = i % nob;
             const bool ok = mbar_wait(&xfull[s], (i / stages) & 1, fail) &&
@@ -418,8 +453,13 @@ __global__ void __launch_bounds__(512)
     uint4 ca = make_uint4(0, 0, 0, 0), cb = ca, na = ca, nb = ca;
     const bool first_slot = (int)threadIdx.x < slots;
     if (n > 0 && first_slot) load(blockIdx.x, threadIdx.x, ca, cb);
-    // x was complete before the layout started; dst_row is the layout's output
-    // (a no-op without a programmatic edge)
+    // x was complete before the layout started: the first token's first slot
+    // is quantised while the layout may still run; dst_row is the layout's
+    // output (the wait is a no-op without a programmatic edge)
+    uint4 q0 = ca;
+    uint32_t sc0 = 0;
+    if constexpr (kFp8)
+        if (n > 0) q0 = quant_slot<Q>(ca, cb, lane, sc0);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int cd = n > 0 && lane < K ? ld_dep(dst_row + (size_t)blockIdx.x * K + lane) : -1;
     float cw = n > 0 && weights ? ld_dep(topk_w + (size_t)blockIdx.x * K + lane) : 0.0f;
@@ -436,14 +476,17 @@ __global__ void __launch_bounds__(512)
         }
         for (int j = threadIdx.x; j - lane < slots; j += blockDim.x) {
             const bool act = j < slots;
-            uint4 a = ca, b = cb;
-            if (j != (int)threadIdx.x) {  // passes beyond the first: loaded here
-                a = b = make_uint4(0, 0, 0, 0);
-                if (act) load(t, j, a, b);
+            uint4 q = q0;
+            uint32_t sc = sc0;
+            if (i > 0 || j != (int)threadIdx.x) {  // (token 0's first slot is done)
+                uint4 a = ca, b = cb;
+                if (j != (int)threadIdx.x) {  // passes beyond the first: loaded here
+                    a = b = make_uint4(0, 0, 0, 0);
+                    if (act) load(t, j, a, b);
+                }
+                q = a;
+                if constexpr (kFp8) q = quant_slot<Q>(a, b, lane, sc);
             }
-            uint4 q = a;
-            uint32_t sc = 0;
-            if constexpr (kFp8) q = quant_slot<Q>(a, b, lane, sc);
             for (int k = 0; k < K; ++k) {  // 16 bytes per lane to each destination
                 const int d = __shfl_sync(kFull, cd, k);
                 if (act && d >= 0) st_v4(out + (size_t)d * row_bytes + (size_t)j * 16, q);
