@@ -36,6 +36,17 @@ WORKLOAD = "dsv3_prefill"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2**20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "combine_dsv3_prefill_traffic.txt")
+# Whole-model serving throughput on 8 GPUs that SGLang PR "[Feature] Add
+# DeepEPv2 (ElasticBuffer) MoE A2A backend" reports in its representative
+# back-to-back serving results (B200 x8, dynamic blockwise FP8 experts), for
+# the DeepEP V2 backend and legacy DeepEP.  Context only: a whole serving
+# stack on 8 GPUs, not a single-GPU dispatch / combine figure.
+PAGES_CONTEXT = {
+    "what": "pages' whole-model serving throughput, 8 GPUs (B200 x8 per the page); "
+            "context only, not comparable with this single-GPU kernel metric",
+    "decode_tok_s": {"deepep_v2": 8429, "legacy_deepep": 8675},
+    "prefill_in_tok_s": {"deepep_v2": 32447, "legacy_deepep": 31533},
+}
 COMBINE_SRC = os.path.join(ROOT, "combine_expert_histogram_gb300", "csrc", "combine.cu")
 
 
@@ -464,6 +475,7 @@ def run_ours(args, w):
         line["rank_dedup"] = measure_rank_dedup(ep, dev)
     if "router" in sections:
         line["router"] = measure_router(ep, dev)
+    line["context"] = PAGES_CONTEXT
     if not args.skip_cpu and world == 1:  # the CPU baseline is an N=1 figure
         line["cpu_baseline"] = cpu_baseline(w, idx, wts, x)
         line["cpu_baseline_threads"] = cpu_baseline_threads(w, idx, wts, x)
