@@ -44,6 +44,8 @@ constexpr int kMaxStages = 8;
 constexpr int kStageBudget = 144 * 1024;  // shared memory per CTA aimed for
 constexpr int kOutBufs = 4;               // FP8 output rows per CTA, at most
 constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory per CTA
+constexpr int kCopyMaxStages = 8;         // bf16 rows in flight per CTA, at most
+constexpr int kCopyBudget = 144 * 1024;   // bf16: shared memory per CTA aimed for
 constexpr long long kWaitLimit = 1LL << 31;  // SM clocks, about a second
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -510,8 +512,8 @@ __global__ void __launch_bounds__(32)
                 uint8_t *__restrict__ out, const float *topk_w, float *__restrict__ row_w,
                 int32_t *status, int stages, int xstage_bytes) {
     extern __shared__ __align__(128) uint8_t smem[];  // [stages] x rows
-    __shared__ __align__(8) uint64_t xfull[kMaxStages];
-    __shared__ int s_loads[kMaxStages];
+    __shared__ __align__(8) uint64_t xfull[kCopyMaxStages];
+    __shared__ int s_loads[kCopyMaxStages];
     const int lane = threadIdx.x;
     const uint32_t row_bytes = 2u * (uint32_t)H;
     const int step = gridDim.x;
@@ -581,13 +583,13 @@ __global__ void __launch_bounds__(32)
     }
 }
 
-// x stages that fit the per-CTA budget beside `fixed` bytes, no more than the
-// tokens one CTA of two per SM would take, at least two.
-int stage_count(int T, int xstage_bytes, int fixed) {
-    int stages = (kStageBudget - fixed) / xstage_bytes;
+// x stages that fit `budget` bytes beside `fixed` ones, no more than the tokens
+// one CTA of two per SM would take, within [2, max_stages].
+int stage_count(int T, int xstage_bytes, int fixed, int budget, int max_stages) {
+    int stages = (budget - fixed) / xstage_bytes;
     const int per_cta = (T + 2 * sm_count() - 1) / (2 * sm_count());
     if (stages > per_cta) stages = per_cta;
-    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages > max_stages) stages = max_stages;
     if (stages < 2) stages = 2;
     return stages;
 }
@@ -595,13 +597,10 @@ int stage_count(int T, int xstage_bytes, int fixed) {
 // Persistent grid: as many CTAs as are resident at once, at most one per token.
 template <typename Kern>
 cudaError_t persistent_grid(Kern kern, int threads, size_t smem, int T, int &grid) {
-    if (smem > 48 * 1024) {
-        cudaError_t err =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-    }
+    cudaError_t err = allow_dynamic_smem(kern, smem);
+    if (err != cudaSuccess) return err;
     int per_sm = 0;
-    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
     if (err != cudaSuccess) return err;
     long long g = (long long)(per_sm > 0 ? per_sm : 1) * sm_count();
     grid = (int)(g < T ? g : T);
@@ -647,7 +646,7 @@ cudaError_t launch_quant(const ep_layout_t &L, const void *x, int H, void *out_r
     const int xstage_bytes = 2 * H;  // H is a multiple of 128
     // output rows: kOutBufs, or 2 where two x stages and kOutBufs rows do not fit
     const int nob = 2 * xstage_bytes + kOutBufs * H <= kSmemMax ? kOutBufs : 2;
-    const int stages = stage_count(T, xstage_bytes, nob * H);
+    const int stages = stage_count(T, xstage_bytes, nob * H, kStageBudget, kMaxStages);
     const size_t smem = (size_t)stages * xstage_bytes + (size_t)nob * H;
     int consumers = (H / 128 * 8 + 31) / 32;  // one slot of 16 elements per lane
     if (consumers > kMaxConsumerWarps) consumers = kMaxConsumerWarps;
@@ -669,7 +668,7 @@ cudaError_t launch_copy(const ep_layout_t &L, const void *x, int H, void *out_ro
                         const float *topk_w, float *row_w, cudaStream_t stream) {
     const int T = L.num_tokens;
     const int xstage_bytes = (2 * H + 127) / 128 * 128;
-    const int stages = stage_count(T, xstage_bytes, 0);
+    const int stages = stage_count(T, xstage_bytes, 0, kCopyBudget, kCopyMaxStages);
     const size_t smem = (size_t)stages * xstage_bytes;
     int grid = 0;
     cudaError_t err = persistent_grid(copy_kernel, 32, smem, T, grid);

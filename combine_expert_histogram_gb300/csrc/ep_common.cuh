@@ -123,6 +123,19 @@ __device__ __forceinline__ void block_exclusive_scan(int n, F value, int32_t *ou
 // Per-device properties, cached on first use (host side).
 int sm_count();
 
+// Let kernel `k` take `dynamic` bytes of dynamic shared memory.  Without an
+// explicit limit a CTA gets 48 KB of shared memory in all, the kernel's static
+// shared memory included, so the limit is raised whenever the two together
+// exceed that.
+template <typename Kern>
+cudaError_t allow_dynamic_smem(Kern k, size_t dynamic) {
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, k);
+    if (err != cudaSuccess) return err;
+    if (dynamic + fa.sharedSizeBytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dynamic);
+}
+
 // Launch with cudaLaunchKernelEx; `programmatic` lets the kernel start while the
 // previous kernel on the stream still runs (programmatic dependent launch): it
 // must then call griddepcontrol.wait before touching that kernel's results.

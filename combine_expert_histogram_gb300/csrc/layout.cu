@@ -358,11 +358,8 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     a.status = L.status;
     cudaError_t err;
     if (p.threads == kSmallThreads) {
-        if (p.smem > 48 * 1024) {
-            err = cudaFuncSetAttribute(assign_kernel<kSmallThreads>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-            if (err != cudaSuccess) return err;
-        }
+        err = allow_dynamic_smem(assign_kernel<kSmallThreads>, p.smem);
+        if (err != cudaSuccess) return err;
         // first kernel of the layout: an ordinary launch, ordered after all prior work
         return launch_kernel(assign_kernel<kSmallThreads>, p.grid, kSmallThreads, p.smem, stream,
                              false, a);
@@ -370,11 +367,8 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     err = launch_kernel(tile_hist_kernel, p.tiles, kTileThreads, sizeof(int32_t) * E, stream,
                         false, topk_idx, TK, E, p.tile, workspace, L.status);
     if (err != cudaSuccess) return err;
-    if (p.smem > 48 * 1024) {
-        err = cudaFuncSetAttribute(assign_kernel<kTileThreads>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-        if (err != cudaSuccess) return err;
-    }
+    err = allow_dynamic_smem(assign_kernel<kTileThreads>, p.smem);
+    if (err != cudaSuccess) return err;
     return launch_kernel(assign_kernel<kTileThreads>, p.grid, kTileThreads, p.smem, stream, true,
                          a);
 }

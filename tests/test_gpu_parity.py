@@ -70,6 +70,16 @@ MID = [
                        layout="masked", quant="fp8_ue8m0", cap=301, seed=17),
     workloads.Workload("h9216_ue8m0", T=1201, H=9216, E=32, K=6, routing="softmax",
                        layout="contig", quant="fp8_ue8m0", align=64, seed=16),
+    # dynamic shared memory of exactly 48 KB, which needs the limit raised
+    # because the kernels also hold static shared memory (on 152 SMs): bf16
+    # dispatch with 8 stages of 6 KB rows, FP8 dispatch with 2 stages + 4 rows
+    # at H=6144, and the single-CTA layout at E=361
+    workloads.Workload("smem48k_bf16", T=2500, H=3072, E=32, K=4, routing="softmax",
+                       layout="contig", quant="none", align=64, seed=18),
+    workloads.Workload("smem48k_fp8", T=400, H=6144, E=64, K=8, routing="softmax",
+                       layout="contig", quant="fp8_ue8m0", align=128, seed=19),
+    workloads.Workload("smem48k_layout", T=128, H=256, E=361, K=8, routing="softmax",
+                       layout="contig", quant="fp8_f32", align=1, seed=20),
     # > 128 tiles of 2048 entries: tiles of several passes
     workloads.Workload("multipass", T=40000, H=128, E=64, K=8, routing="softmax",
                        layout="contig", quant="fp8_ue8m0", align=128, R=4, seed=10),
@@ -211,3 +221,19 @@ def test_masked_repack_vs_oracle_with_overflow():
     assert np.array_equal(slab.reshape(w.E * cap, -1).cpu().numpy(), o_slab)
     m = np.repeat(np.arange(cap)[None, :] < o_mm[:, None], 1).reshape(-1)
     assert np.array_equal(slab_sc.reshape(w.E * cap, -1).cpu().numpy()[m], o_ss[m])
+
+
+@pytest.mark.parametrize("quant", ["fp8_ue8m0", "none", "mxfp8"])
+def test_dispatch_kernel_boundary(quant):
+    """Dispatch picks its kernel by load: registers up to 2 tokens per SM, the
+    shared-memory ring above.  Both sides of the boundary match the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for T in (2 * sms, 2 * sms + 1):
+        w = workloads.Workload(f"boundary_{quant}_{T}", T=T, H=7168, E=64, K=8,
+                               routing="softmax", layout="masked" if quant == "fp8_ue8m0" else "contig",
+                               quant=quant, align=128, cap=T, seed=T)
+        case = gh.make_case(w)
+        g = gh.run_gpu(w, case)
+        ref = gh.check_layout(w, case, g)
+        gh.check_dispatch(w, case, g, ref)
+        assert gh.check_combine(w, case, g, ref) == 1.0
