@@ -690,8 +690,9 @@ def measure_e2e(ep, w, L, idx, wts, x, y_dev, out_rows, out_scales, dev, stream,
     runs layout + dispatch + combine and copies the combined output (and the
     expert histogram) back.  Steps are pipelined the way a serving loop would
     run them: inputs are double-buffered on the device, so step i+1's inputs
-    travel host->device while step i computes and its output travels back
-    (the host link is full duplex)."""
+    travel host->device while step i computes and its output travels back.
+    Uploads and downloads together are bound by the host link (about 211 GB/s
+    measured for both directions combined)."""
     import torch
     pin = dict(pin_memory=True)
     h_idx = torch.from_numpy(idx).pin_memory()
