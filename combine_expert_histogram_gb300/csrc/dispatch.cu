@@ -47,7 +47,6 @@ constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory per CTA
 constexpr int kCopyMaxStages = 8;         // bf16 rows in flight per CTA, at most
 constexpr int kCopyBudget = 144 * 1024;   // bf16: shared memory per CTA aimed for
 constexpr long long kWaitLimit = 1LL << 31;  // SM clocks, about a second
-constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d) {
     // __nv_cvt_float2_to_fp8x2: round to nearest even, saturate to +-448;
@@ -198,7 +197,7 @@ __device__ __forceinline__ void store_scales(uint32_t *scales, uint32_t sc, int 
         // group j/8's scale: lane sub of the group writes it for k = sub, sub+8, ...
         for (int kb = 0; kb < K; kb += 8) {
             const int k = kb + (lane & 7);
-            const int d = __shfl_sync(kFull, cd, k & 31);
+            const int d = __shfl_sync(kFullMask, cd, k & 31);
             if (j < slots && k < K && d >= 0) scales[(size_t)d * G + (j >> 3)] = sc;
         }
     } else if constexpr (Q == EP_QUANT_MXFP8) {
@@ -207,11 +206,11 @@ __device__ __forceinline__ void store_scales(uint32_t *scales, uint32_t sc, int 
         const int wi = lane >> 3;
         uint32_t word = 0;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) word |= __shfl_sync(kFull, sc, 8 * wi + 2 * m) << (8 * m);
+        for (int m = 0; m < 4; ++m) word |= __shfl_sync(kFullMask, sc, 8 * wi + 2 * m) << (8 * m);
         const int g = (wbase >> 3) + wi;  // the word's index in the scale row
         for (int kb = 0; kb < K; kb += 8) {
             const int k = kb + (lane & 7);
-            const int d = __shfl_sync(kFull, cd, k & 31);
+            const int d = __shfl_sync(kFullMask, cd, k & 31);
             if (g < G && k < K && d >= 0) scales[(size_t)d * G + g] = word;
         }
     } else {
@@ -220,7 +219,7 @@ __device__ __forceinline__ void store_scales(uint32_t *scales, uint32_t sc, int 
         uint32_t word = 0;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const uint32_t e = __shfl_sync(kFull, sc, 8 * m);
+            const uint32_t e = __shfl_sync(kFullMask, sc, 8 * m);
             word |= ((wbase >> 3) + m < G ? e : 127u) << (8 * m);
         }
         const int wd = wbase >> 5;
@@ -295,13 +294,13 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
             const int nd = i + 1 < n && lane < K ? ld_dep(dst_row + (size_t)(t + step) * K + lane) : -1;
             const int b = i % nob;
             const bool ok = mbar_wait(&ofull[b], (i / nob) & 1, fail);
-            if (__any_sync(kFull, !ok)) {  // the whole warp leaves together
+            if (__any_sync(kFullMask, !ok)) {  // the whole warp leaves together
                 s_fail = 1;
                 break;
             }
             const uint8_t *orow = orows + (size_t)b * H;
             for (int k = 0; k < K; ++k) {
-                const int d = __shfl_sync(kFull, cd, k);
+                const int d = __shfl_sync(kFullMask, cd, k);
                 if (lane == 0 && d >= 0) bulk_store(out + (size_t)d * H, orow, (uint32_t)H);
             }
             if (lane == 0) {
@@ -314,7 +313,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
             if (i + stages < n) {  // refill this token's x stage once every consumer read it
                 const int s = i % stages;
                 const bool ok2 = mbar_wait(&xempty[s], (i / stages) & 1, fail);
-                if (__any_sync(kFull, !ok2)) {
+                if (__any_sync(kFullMask, !ok2)) {
                     s_fail = 1;
                     break;
                 }
@@ -339,7 +338,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
         uint32_t sc0 = 0;
         if (early) {
             const bool ok = mbar_wait(&xfull[0], 0, fail);  // output row 0 starts free
-            if (__any_sync(kFull, !ok)) {
+            if (__any_sync(kFullMask, !ok)) {
                 s_fail = 1;
                 early = false;
             } else {
@@ -380,7 +379,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
             const int s = i % stages, b = i % nob;
             const bool ok = mbar_wait(&xfull[s], (i / stages) & 1, fail) &&
                             mbar_wait(&oempty[b], ((i / nob) & 1) ^ 1, fail);
-            if (__any_sync(kFull, !ok)) {  // the whole warp leaves together
+            if (__any_sync(kFullMask, !ok)) {  // the whole warp leaves together
                 s_fail = 1;
                 break;
             }
@@ -490,7 +489,7 @@ __global__ void __launch_bounds__(512)
                 if constexpr (kFp8) q = quant_slot<Q>(a, b, lane, sc);
             }
             for (int k = 0; k < K; ++k) {  // 16 bytes per lane to each destination
-                const int d = __shfl_sync(kFull, cd, k);
+                const int d = __shfl_sync(kFullMask, cd, k);
                 if (act && d >= 0) st_v4(out + (size_t)d * row_bytes + (size_t)j * 16, q);
             }
             if constexpr (kFp8)
@@ -544,13 +543,13 @@ __global__ void __launch_bounds__(32)
             if (weights) nw = ld_dep(topk_w + (size_t)(t + step) * K + lane);
         }
         const int s = i % stages;
-        if (__any_sync(kFull, !mbar_wait(&xfull[s], (i / stages) & 1, nullptr))) {
+        if (__any_sync(kFullMask, !mbar_wait(&xfull[s], (i / stages) & 1, nullptr))) {
             failed = true;
             break;
         }
         const uint8_t *row = smem + (size_t)s * xstage_bytes;
         for (int k = 0; k < K; ++k) {
-            const int d = __shfl_sync(kFull, cd, k);
+            const int d = __shfl_sync(kFullMask, cd, k);
             if (lane == 0 && d >= 0) bulk_store(out + (size_t)d * row_bytes, row, row_bytes);
         }
         if (lane == 0) {
