@@ -165,7 +165,9 @@ struct LayoutPlan {
     int tile;         // entries per tile
     int grid;         // CTAs of the assign kernel (>= tiles; extra CTAs fill padding)
     size_t smem;      // dynamic shared memory of the assign kernel
-    size_t ws_bytes;  // scratch: tiles x E int32 per-tile histograms (0 when tiles == 1)
+    size_t ws_bytes;  // scratch: tiles x E int32 per-tile histograms (0 when tiles == 1
+                      // or self_hist)
+    bool self_hist;   // several tiles, one kernel: every CTA recounts all entries itself
 };
 LayoutPlan layout_plan(const ep_layout_t &L);
 cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t *workspace,

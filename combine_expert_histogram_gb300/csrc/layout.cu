@@ -16,12 +16,16 @@
 //     the mask is kept per round and reused for ranking;
 //   * up to 1024 entries one 1024-thread CTA does everything in one kernel;
 //     above that, tiles of 1024 entries (2048 beyond 32768) on 256-thread
-//     CTAs, so that the ballot work of decode-sized batches spreads over SMs:
-//     tile_hist_kernel counts each tile's experts (shared-memory atomics;
-//     counts need no order) into the scratch workspace [tiles][E], then
-//     assign_kernel (launched as a programmatic dependent, so its loads and
-//     ballots overlap tile_hist) waits for it and sums the workspace columns
-//     into the expert totals and its tile's base;
+//     CTAs, so that the ballot work of decode-sized batches spreads over SMs;
+//   * up to 4096 entries the tiles still run as one kernel: every tile CTA
+//     recounts all entries with shared-memory atomics (a few per thread) for
+//     the expert totals and its tile's base, so no CTA depends on another and
+//     CTA 0 alone writes the status word;
+//   * beyond that, tile_hist_kernel counts each tile's experts (shared-memory
+//     atomics; counts need no order) into the scratch workspace [tiles][E],
+//     then assign_kernel (launched as a programmatic dependent, so its loads
+//     and ballots overlap tile_hist) waits for it and sums the workspace
+//     columns into the expert totals and its tile's base;
 //   * assign_kernel scans the padded counts, turns per-warp histograms into
 //     per-warp starting slots and gives each entry
 //     slot = warp base + #lower lanes with the same expert: exactly ascending
@@ -40,6 +44,7 @@ constexpr int kSumChunk = 16;    // workspace loads in flight per thread
 constexpr int kSmallThreads = 1024;                     // single-tile CTA
 constexpr int kTileThreads = 256;                       // multi-tile CTAs
 constexpr int kSmallMax = kSmallThreads;                // 1024 entries: one round per warp
+constexpr int kSelfHistMax = 4096;  // up to here every tile CTA recounts all entries itself
 
 __host__ __device__ inline int round_up_pow2(int v, int a) { return (v + a - 1) & ~(a - 1); }
 
@@ -116,7 +121,8 @@ struct AssignArgs {
     int chunk;   // entries per warp per pass (multiple of 32, <= kChunk)
     int passes;  // passes per tile
     int tile, tiles;
-    const int32_t *ws;  // [tiles][E]; unused when tiles == 1
+    int self_hist;      // tiles > 1 without the histogram kernel (see layout_plan)
+    const int32_t *ws;  // [tiles][E]; unused when tiles == 1 or self_hist
     int32_t *dst_row, *row_src, *count, *offset, *rank_rows, *status;
 };
 
@@ -129,6 +135,7 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
     int32_t *wh = sm;                         // [passes][kWarps][E]: per-warp counts, then slot bases
     int32_t *tot = wh + passes * kWarps * E;  // [E] expert histogram
     int32_t *off = tot + E;                   // [E+1] first row of each expert
+    int32_t *pre = off + E + 1;               // [E] self_hist: entries before this tile
     __shared__ int32_t scan_tmp[kWarps];
 
     pdl_launch_dependents();  // dispatch may start loading and quantising x now
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
     if (!assigns) {
         // Fill CTA (masked layouts with row_src): only the expert counts are
         // needed, in any order; masked offsets are e*cap, so no scan either.
-        if (a.tiles == 1) {
+        if (a.tiles == 1 || a.self_hist) {
             for (int e = threadIdx.x; e < E; e += NT) tot[e] = 0;
             __syncthreads();
             for (int i = threadIdx.x; i < a.TK; i += NT) {
@@ -167,6 +174,34 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
     }
 
     for (int j = threadIdx.x; j < passes * kWarps * E; j += NT) wh[j] = 0;
+    if (a.self_hist) {
+        // No histogram kernel: every tile CTA recounts all entries (a few
+        // shared-memory atomics per thread at these sizes): the expert totals
+        // and the entries before its own tile.  Done first, so that the chunk
+        // loads below find this tile's entries in L1.  Every CTA thus sees
+        // every bad id and every over-full expert, so CTA 0 alone writes the
+        // status word, once, and no CTA raises errors into it.
+        for (int e = threadIdx.x; e < E; e += NT) tot[e] = pre[e] = 0;
+        __syncthreads();
+        int bad = 0;
+        for (int i = threadIdx.x; i < a.TK; i += NT) {
+            const int e = __ldg(a.idx + i);
+            if (e >= 0 && e < E) {
+                atomicAdd(&tot[e], 1);
+                if (i < start) atomicAdd(&pre[e], 1);
+            } else if (e != -1) {
+                bad = 1;
+            }
+        }
+        bad = __syncthreads_or(bad);
+        int over = 0;
+        if (a.masked)
+            for (int e = threadIdx.x; e < E; e += NT) over |= tot[e] > a.cap;
+        over = __syncthreads_or(over);
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            *a.status = bad ? EP_ERR_BAD_EXPERT_ID : over ? EP_ERR_CAPACITY : EP_OK;
+    }
+
     __syncthreads();
 
     // 1. per-(pass, warp) expert histogram of this tile; chunks stay in
@@ -195,7 +230,10 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
     // 2. expert totals and this tile's base; per-warp counts -> starting slots
     for (int e = threadIdx.x; e < E; e += NT) {
         int total = 0, base = 0;
-        if (a.tiles == 1) {
+        if (a.self_hist) {
+            total = tot[e];
+            base = pre[e];
+        } else if (a.tiles == 1) {
             for (int j = 0; j < passes * kWarps; ++j) total += wh[j * E + e];
         } else {
             for (int b0 = 0; b0 < a.tiles; b0 += kSumChunk) {
@@ -266,12 +304,13 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
                 if (i < c1) {
                     int dst = -1;
                     if (c.bad & (1u << r)) {
-                        raise_status(a.status, EP_ERR_BAD_EXPERT_ID);
+                        if (!a.self_hist) raise_status(a.status, EP_ERR_BAD_EXPERT_ID);
                     } else if (e < E) {
-                        if (masked && slot >= cap)
-                            raise_status(a.status, EP_ERR_CAPACITY);
-                        else
+                        if (masked && slot >= cap) {
+                            if (!a.self_hist) raise_status(a.status, EP_ERR_CAPACITY);
+                        } else {
                             dst = off[e] + slot;
+                        }
                     }
                     a.dst_row[i] = dst;
                     if (dst >= 0 && a.row_src) a.row_src[dst] = i;
@@ -322,13 +361,16 @@ LayoutPlan layout_plan(const ep_layout_t &L) {
         p.tiles = (int)tiles;
         p.tile = (int)pass_len * p.passes;
     }
+    // few tiles: one kernel, each tile CTA recounting every entry, instead of
+    // a histogram kernel and a workspace (a kernel boundary saved on decode)
+    p.self_hist = p.tiles > 1 && TK <= kSelfHistMax;
     const bool fill = L.kind == EP_LAYOUT_MASKED && L.row_src != nullptr;
     p.grid = p.tiles;
     if (fill && p.grid < kFillCtas) p.grid = L.num_experts < kFillCtas ? L.num_experts : kFillCtas;
     if (p.grid < p.tiles) p.grid = p.tiles;
-    p.smem = sizeof(int32_t) *
-             ((size_t)p.passes * warps * L.num_experts + 2 * (size_t)L.num_experts + 1);
-    p.ws_bytes = p.tiles > 1 ? sizeof(int32_t) * (size_t)p.tiles * L.num_experts : 0;
+    p.smem = sizeof(int32_t) * ((size_t)p.passes * warps * L.num_experts +
+                                (p.self_hist ? 3 : 2) * (size_t)L.num_experts + 1);
+    p.ws_bytes = p.tiles > 1 && !p.self_hist ? sizeof(int32_t) * (size_t)p.tiles * L.num_experts : 0;
     return p;
 }
 
@@ -349,6 +391,7 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     a.passes = p.passes;
     a.tile = p.tile;
     a.tiles = p.tiles;
+    a.self_hist = p.self_hist;
     a.ws = workspace;
     a.dst_row = L.dst_row;
     a.row_src = L.row_src;
@@ -362,6 +405,12 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
         if (err != cudaSuccess) return err;
         // first kernel of the layout: an ordinary launch, ordered after all prior work
         return launch_kernel(assign_kernel<kSmallThreads>, p.grid, kSmallThreads, p.smem, stream,
+                             false, a);
+    }
+    if (p.self_hist) {  // the only kernel: an ordinary launch
+        err = allow_dynamic_smem(assign_kernel<kTileThreads>, p.smem);
+        if (err != cudaSuccess) return err;
+        return launch_kernel(assign_kernel<kTileThreads>, p.grid, kTileThreads, p.smem, stream,
                              false, a);
     }
     err = launch_kernel(tile_hist_kernel, p.tiles, kTileThreads, sizeof(int32_t) * E, stream,

@@ -26,7 +26,8 @@ def _guards_intact(buf, n):
     return bool((buf[:GUARD] == PAT).all()) and bool((buf[GUARD + n:] == PAT).all())
 
 
-@pytest.mark.parametrize("T", [50, 3000])  # one tile and several tiles
+# one tile; several tiles in one kernel; a histogram kernel + assign kernel
+@pytest.mark.parametrize("T", [50, 500, 3000, 5000])
 def test_bad_expert_ids_raise_status_without_stray_writes(T):
     E, K = 16, 4
     rng = np.random.default_rng(0)
@@ -50,7 +51,7 @@ def test_bad_expert_ids_raise_status_without_stray_writes(T):
     assert _guards_intact(rs_buf, rows) and _guards_intact(dr_buf, T * K)
 
 
-@pytest.mark.parametrize("T", [40, 4000])
+@pytest.mark.parametrize("T", [40, 700, 4000, 4500])
 def test_masked_capacity_overflow(T):
     E, K, cap = 8, 4, 9
     rng = np.random.default_rng(1)
@@ -91,3 +92,25 @@ def test_status_resets_on_next_layout():
     ep.ep_layout(good, E, align=4, out=L)
     torch.cuda.synchronize()
     assert int(L.status.item()) == 0
+
+
+@pytest.mark.parametrize("T", [300, 3000])  # several tiles: one kernel; two kernels
+def test_multi_tile_status_max_and_reset(T):
+    """Bad ids and an over-full masked expert together report the larger code;
+    the next layout of good ids resets it."""
+    E, K, cap = 16, 8, 8
+    rng = np.random.default_rng(2)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    idx[T // 2, 5] = E + 3
+    L = ep.new_layout(T, K, E, "masked", capacity=cap)
+    ep.ep_layout(torch.from_numpy(idx).cuda(), E, kind="masked", capacity=cap, out=L)
+    torch.cuda.synchronize()
+    ref = oracle.default().layout(idx, E, "masked", cap=cap)
+    assert int(L.status.item()) == ref["status"] == ep.EP_ERR_BAD_EXPERT_ID
+    assert np.array_equal(L.dst_row.cpu().numpy().reshape(T, K), ref["dst_row"])
+    good = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    L2 = ep.new_layout(T, K, E, "masked", capacity=T)
+    L2.status = L.status  # the status word still holds the error
+    ep.ep_layout(torch.from_numpy(good).cuda(), E, kind="masked", capacity=T, out=L2)
+    torch.cuda.synchronize()
+    assert int(L2.status.item()) == 0
