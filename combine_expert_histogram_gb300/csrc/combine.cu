@@ -4,13 +4,18 @@
 // ElasticBuffer support to MoE token dispatcher", section "Motivation").
 //
 // out[t, h] = bf16_rn( sum_{k ascending, dst_row[t,k] >= 0} w[t,k] * y[dst_row[t,k], h] )
-// with fp32 products and sums each rounded separately (__fmul_rn / __fadd_rn,
-// so no fused multiply-add), starting from +0.
+// with fp32 products and sums each rounded separately (no fused multiply-add),
+// starting from +0.  The products come two at a time from packed f32x2
+// multiplies (each lane an IEEE round-to-nearest multiply); the sums stay
+// scalar __fadd_rn: with a packed add consuming a packed product, the compiler
+// was measured to contract the pair into a fused multiply-add (results then
+// differ from separate rounding in cancelling sums).
 //
 // HBM-bound gather: one lane owns 8 output elements (16 bytes) of one token;
 // a warp covers 256 consecutive elements, so each of its K row loads is 512
 // contiguous bytes.  The lane first issues all loads of a batch of 8 entries
-// (8 x 16 B in flight per lane), then reduces them in k order.
+// (8 x 16 B in flight per lane), then reduces them in k order.  The token's
+// destinations and weights come as 16-byte loads where K allows.
 #include <cuda_bf16.h>
 
 #include "ep_common.cuh"
@@ -21,6 +26,29 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBatch = 8;
 
+// Two fp32 lanes in one 64-bit register (element 0 in the low half), and the
+// packed sm_100+ multiply on them: each lane is an IEEE round-to-nearest
+// multiply, exactly what __fmul_rn gives per element.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float2 split_f32x2(uint64_t a) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(a));
+    return r;
+}
+
+// kVec: K is a multiple of 4 and dst_row / topk_w are 16-byte aligned, so a
+// token's destinations and weights arrive as 16-byte loads (4 entries each)
+// instead of one load per entry.
+template <bool kVec>
 __global__ void __launch_bounds__(kThreads)
     combine_kernel(const uint16_t *y, int K, int H, long long n_chunks, const int32_t *dst_row,
                    const float *topk_w, uint16_t *__restrict__ out) {
@@ -35,19 +63,32 @@ __global__ void __launch_bounds__(kThreads)
     const int32_t *drow = dst_row + (size_t)t * K;
     const float *wrow = topk_w + (size_t)t * K;
 
-    float acc[8];
+    uint64_t acc[4];  // output pairs (8i, 8i+1): fp32, from +0
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < 4; ++i) acc[i] = 0;
 
     for (int k0 = 0; k0 < K; k0 += kBatch) {
         int d[kBatch];
         float w[kBatch];
         uint4 v[kBatch];
+        if (kVec) {
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int k = k0 + u;
-            d[u] = k < K ? ld_dep(drow + k) : -1;
-            w[u] = k < K ? ld_dep(wrow + k) : 0.0f;
+            for (int q = 0; q < kBatch / 4; ++q) {
+                const bool in = k0 + 4 * q < K;  // whole quads: K % 4 == 0
+                const uint4 dq = in ? ld_dep_v4(drow + k0 + 4 * q) : make_uint4(~0u, ~0u, ~0u, ~0u);
+                const uint4 wq = in ? ld_dep_v4(wrow + k0 + 4 * q) : make_uint4(0, 0, 0, 0);
+                d[4 * q] = (int)dq.x, d[4 * q + 1] = (int)dq.y, d[4 * q + 2] = (int)dq.z,
+                d[4 * q + 3] = (int)dq.w;
+                w[4 * q] = __uint_as_float(wq.x), w[4 * q + 1] = __uint_as_float(wq.y),
+                w[4 * q + 2] = __uint_as_float(wq.z), w[4 * q + 3] = __uint_as_float(wq.w);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int k = k0 + u;
+                d[u] = k < K ? ld_dep(drow + k) : -1;
+                w[u] = k < K ? ld_dep(wrow + k) : 0.0f;
+            }
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
@@ -55,18 +96,21 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             if (d[u] < 0) continue;
+            const uint64_t w2 = f32x2(w[u], w[u]);
             const uint32_t p[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w[u], bf16_lo(p[i])));
-                acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w[u], bf16_hi(p[i])));
+                const float2 m = split_f32x2(mul_f32x2(w2, f32x2(bf16_lo(p[i]), bf16_hi(p[i]))));
+                const float2 a = split_f32x2(acc[i]);
+                acc[i] = f32x2(__fadd_rn(a.x, m.x), __fadd_rn(a.y, m.y));
             }
         }
     }
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        const float2 a = split_f32x2(acc[i]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(a.x, a.y);
         o[i] = *reinterpret_cast<const uint32_t *>(&b);  // .x (first) in the low half
     }
     st_v4(out + (size_t)t * H + j * 8, make_uint4(o[0], o[1], o[2], o[3]));
@@ -80,9 +124,14 @@ cudaError_t launch_combine(const ep_layout_t &L, const void *y, int H, const flo
     if (T == 0) return cudaSuccess;
     const long long n = (long long)T * (H / 8);
     const long long blocks = (n + kThreads - 1) / kThreads;
-    return launch_kernel(combine_kernel, (int)blocks, kThreads, 0, stream, true,
-                         static_cast<const uint16_t *>(y), K, H, n, L.dst_row, topk_w,
-                         static_cast<uint16_t *>(out));
+    const bool vec = K % 4 == 0 && reinterpret_cast<uintptr_t>(L.dst_row) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(topk_w) % 16 == 0;
+    return vec ? launch_kernel(combine_kernel<true>, (int)blocks, kThreads, 0, stream, true,
+                               static_cast<const uint16_t *>(y), K, H, n, L.dst_row, topk_w,
+                               static_cast<uint16_t *>(out))
+               : launch_kernel(combine_kernel<false>, (int)blocks, kThreads, 0, stream, true,
+                               static_cast<const uint16_t *>(y), K, H, n, L.dst_row, topk_w,
+                               static_cast<uint16_t *>(out));
 }
 
 }  // namespace ep

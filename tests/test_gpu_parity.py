@@ -5,6 +5,7 @@ import torch
 
 import oracle
 import workloads
+from combine_expert_histogram_gb300 import binding as ep
 from tests import gpu_harness as gh
 
 pytestmark = pytest.mark.gpu
@@ -237,3 +238,29 @@ def test_dispatch_kernel_boundary(quant):
         ref = gh.check_layout(w, case, g)
         gh.check_dispatch(w, case, g, ref)
         assert gh.check_combine(w, case, g, ref) == 1.0
+
+
+@pytest.mark.parametrize("K", [16, 13])  # 16-byte index loads; scalar index loads
+def test_combine_cancelling_sums_bit_exact(K):
+    """Entries k and k + K//2 of a token carry the same weight and opposite
+    expert rows, so every sum nearly cancels and only separately rounded
+    products and sums reproduce the oracle's bits; a fused multiply-add (or any
+    other reordering) shows up here at once."""
+    T, H, E = 2048, 1024, 64
+    half = K // 2
+    rng = np.random.default_rng(77)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    wts = rng.random((T, K)).astype(np.float32)
+    wts[:, half:2 * half] = wts[:, :half]
+    orc = oracle.default()
+    ref = orc.layout(idx, E, "contig", align=1)
+    rows, dst = ref["rows"], ref["dst_row"]
+    x = rng.standard_normal((rows, H)).astype(np.float32)
+    y_bits = (x.view(np.uint32) >> 16).astype(np.uint16)  # truncate to bf16
+    y_bits[dst[:, half:2 * half].ravel()] = y_bits[dst[:, :half].ravel()] ^ 0x8000  # exact negation
+    y = torch.from_numpy(y_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    L = ep.ep_layout(torch.from_numpy(idx).cuda(), E, kind="contig", align=1)
+    out = ep.ep_combine(L, y, torch.from_numpy(wts).cuda())
+    torch.cuda.synchronize()
+    expect = orc.combine(y_bits, wts, dst, H)
+    assert np.array_equal(gh.to_np_u16(out), expect)
