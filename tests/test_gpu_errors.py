@@ -114,3 +114,25 @@ def test_multi_tile_status_max_and_reset(T):
     ep.ep_layout(torch.from_numpy(good).cuda(), E, kind="masked", capacity=T, out=L2)
     torch.cuda.synchronize()
     assert int(L2.status.item()) == 0
+
+
+# one CTA; tiles in one kernel; histogram kernel + assign kernel
+@pytest.mark.parametrize("cap", [64, 800, 2500])
+def test_masked_capacity_exact_boundary(cap):
+    """An expert receiving exactly `capacity` rows is fine; one row more raises
+    EP_ERR_CAPACITY and only the extra entry goes unplaced."""
+    E, K = 16, 4
+    rng = np.random.default_rng(cap)
+    for extra in (0, 1):
+        T = cap + extra
+        idx = np.stack([np.concatenate([[0], 1 + rng.permutation(E - 1)[:K - 1]])
+                        for _ in range(T)]).astype(np.int32)  # expert 0 in every token
+        L = ep.new_layout(T, K, E, "masked", capacity=cap)
+        ep.ep_layout(torch.from_numpy(idx).cuda(), E, kind="masked", capacity=cap, out=L)
+        torch.cuda.synchronize()
+        ref = oracle.default().layout(idx, E, "masked", cap=cap)
+        assert int(L.status.item()) == ref["status"] == (ep.EP_ERR_CAPACITY if extra else 0)
+        got = L.dst_row.cpu().numpy().reshape(T, K)
+        assert np.array_equal(got, ref["dst_row"])
+        assert int((got[:, 0] < 0).sum()) == extra  # only the last token's expert-0 entry
+        assert int(L.expert_count.cpu()[0]) == T
