@@ -23,7 +23,7 @@
 namespace ep {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kBatch = 8;
 
 // Two fp32 lanes in one 64-bit register (element 0 in the low half), and the
