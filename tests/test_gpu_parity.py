@@ -264,3 +264,30 @@ def test_combine_cancelling_sums_bit_exact(K):
     torch.cuda.synchronize()
     expect = orc.combine(y_bits, wts, dst, H)
     assert np.array_equal(gh.to_np_u16(out), expect)
+
+
+@pytest.mark.parametrize("shift", ["dst_row", "topk_w"])
+def test_combine_index_arrays_not_16_byte_aligned(shift):
+    """K % 4 == 0 but one index array only 4-byte aligned: combine must take
+    the one-entry-at-a-time loads and still match the oracle bit for bit."""
+    w = workloads.Workload("align4", T=777, H=512, E=32, K=8, routing="softmax",
+                           layout="contig", quant="none", align=16, seed=23)
+    case = gh.make_case(w)
+    L = ep.ep_layout(case["idx_d"], w.E, kind="contig", align=w.align)
+    wts = case["w_d"]
+    if shift == "dst_row":
+        buf = torch.empty(L.dst_row.numel() + 1, dtype=torch.int32, device="cuda")
+        buf[1:].copy_(L.dst_row)
+        L.dst_row = buf[1:]
+    else:
+        buf = torch.empty(wts.numel() + 1, dtype=torch.float32, device="cuda")
+        buf[1:].copy_(wts.view(-1))
+        wts = buf[1:].view(wts.shape)
+    y = workloads.make_expert_outputs(L.rows_capacity, w.H, seed=3, device="cuda")
+    out = ep.ep_combine(L, y, wts)
+    torch.cuda.synchronize()
+    ref = oracle.default().layout(case["idx"], w.E, "contig", align=w.align)
+    dst = ref["dst_row"]
+    y_bits = gh.to_np_u16(y)
+    expect = oracle.default().combine(y_bits, case["w"], dst, w.H)
+    assert np.array_equal(gh.to_np_u16(out), expect)
