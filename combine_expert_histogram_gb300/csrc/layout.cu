@@ -56,14 +56,19 @@ struct Chunk {
     unsigned bad;
 };
 
-__device__ __forceinline__ void load_chunk(const int32_t *__restrict__ idx, int c0, int c1,
-                                           int E, int nbits, Chunk &c) {
+// Issue the chunk's loads (entries past c1 read as -1).
+__device__ __forceinline__ void fetch_chunk(const int32_t *__restrict__ idx, int c0, int c1,
+                                            Chunk &c) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
         const int i = c0 + r * 32 + lane;
         c.ev[r] = i < c1 ? __ldg(idx + i) : -1;
     }
+}
+
+// Map invalid ids to E (recording bad ones) and find each round's peers.
+__device__ __forceinline__ void classify_chunk(int c0, int c1, int E, int nbits, Chunk &c) {
     c.bad = 0;
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
@@ -86,6 +91,42 @@ __device__ __forceinline__ void load_chunk(const int32_t *__restrict__ idx, int 
         }
         c.peers[r] = m;
     }
+}
+
+__device__ __forceinline__ void load_chunk(const int32_t *__restrict__ idx, int c0, int c1,
+                                           int E, int nbits, Chunk &c) {
+    fetch_chunk(idx, c0, c1, c);
+    classify_chunk(c0, c1, E, nbits, c);
+}
+
+// Expert totals (and, when pre != nullptr, the entries before `start`) of
+// the first TK entries, by shared-memory atomics; loads are issued eight at a
+// time ahead of their atomics.  Returns 1 if this thread saw an id outside
+// [-1, E).
+template <int NT>
+__device__ __forceinline__ int count_all(const int32_t *__restrict__ idx, int TK, int E, int start,
+                                         int32_t *tot, int32_t *pre) {
+    constexpr int kBatchLoads = 8;
+    int bad = 0;
+    for (int i0 = threadIdx.x; i0 < TK; i0 += NT * kBatchLoads) {
+        int ev[kBatchLoads];
+#pragma unroll
+        for (int u = 0; u < kBatchLoads; ++u) {
+            const int i = i0 + u * NT;
+            ev[u] = i < TK ? __ldg(idx + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatchLoads; ++u) {
+            const int i = i0 + u * NT, e = ev[u];
+            if (e >= 0 && e < E) {
+                atomicAdd(&tot[e], 1);
+                if (pre && i < start) atomicAdd(&pre[e], 1);
+            } else if (e != -1 && i < TK) {
+                bad = 1;
+            }
+        }
+    }
+    return bad;
 }
 
 __device__ __forceinline__ int id_bits(int E) { return 32 - __clz(E); }  // E itself must fit
@@ -154,10 +195,7 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
         if (a.tiles == 1 || a.self_hist) {
             for (int e = threadIdx.x; e < E; e += NT) tot[e] = 0;
             __syncthreads();
-            for (int i = threadIdx.x; i < a.TK; i += NT) {
-                const int e = __ldg(a.idx + i);
-                if (e >= 0 && e < E) atomicAdd(&tot[e], 1);
-            }
+            count_all<NT>(a.idx, a.TK, E, 0, tot, nullptr);
         } else {
             pdl_wait();
             for (int e = threadIdx.x; e < E; e += NT) {
@@ -173,6 +211,11 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
         return;
     }
 
+    // single-pass tiles: the chunk's loads go out first, so that their latency
+    // overlaps the zeroing (and the recount) below
+    Chunk c;
+    if (passes == 1)
+        fetch_chunk(a.idx, start + warp * a.chunk, min(end, start + warp * a.chunk + a.chunk), c);
     for (int j = threadIdx.x; j < passes * kWarps * E; j += NT) wh[j] = 0;
     if (a.self_hist) {
         // No histogram kernel: every tile CTA recounts all entries (a few
@@ -183,17 +226,7 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
         // status word, once, and no CTA raises errors into it.
         for (int e = threadIdx.x; e < E; e += NT) tot[e] = pre[e] = 0;
         __syncthreads();
-        int bad = 0;
-        for (int i = threadIdx.x; i < a.TK; i += NT) {
-            const int e = __ldg(a.idx + i);
-            if (e >= 0 && e < E) {
-                atomicAdd(&tot[e], 1);
-                if (i < start) atomicAdd(&pre[e], 1);
-            } else if (e != -1) {
-                bad = 1;
-            }
-        }
-        bad = __syncthreads_or(bad);
+        const int bad = __syncthreads_or(count_all<NT>(a.idx, a.TK, E, start, tot, pre));
         int over = 0;
         if (a.masked)
             for (int e = threadIdx.x; e < E; e += NT) over |= tot[e] > a.cap;
@@ -206,12 +239,14 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
 
     // 1. per-(pass, warp) expert histogram of this tile; chunks stay in
     //    registers for single-pass tiles (the common case), else are reloaded.
-    Chunk c;
     {
         for (int p = 0; p < passes; ++p) {
             const int c0 = start + p * pass_len + warp * a.chunk;
             const int c1 = min(end, c0 + a.chunk);
-            load_chunk(a.idx, c0, c1, E, nbits, c);
+            if (passes == 1)
+                classify_chunk(c0, c1, E, nbits, c);
+            else
+                load_chunk(a.idx, c0, c1, E, nbits, c);
             int32_t *row = wh + (p * kWarps + warp) * E;
 #pragma unroll
             for (int r = 0; r < kRounds; ++r) {
