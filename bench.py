@@ -544,12 +544,15 @@ def measure_decode(ep, dev, reps=10):
         lay = lambda: ep.ep_layout(idx_d, w.E, out=L, stream=s)
         dis = lambda: ep.ep_dispatch(L, x_d, w.quant, out_rows=out_rows, out_scales=sc, stream=s)
         com = lambda: ep.ep_combine(L, y, w_d, out=out, stream=s)
+        fus = lambda: ep.ep_layout_dispatch(idx_d, L, x_d, w.quant, out_rows=out_rows,
+                                            out_scales=sc, stream=s)
         flush = lambda: flush_buf.fill_(1)
         with torch.cuda.stream(s):
             for _ in range(3):
-                lay(), dis(), com()
+                lay(), dis(), com(), fus(), com()
         torch.cuda.synchronize()
         step_us = graph_time_us([lay, dis, com], s, reps)
+        fused_us = graph_time_us([fus, com], s, reps)  # layout + dispatch in one call
         cold = {k: graph_time_us([f], s, reps, flush=flush)
                 for k, f in (("layout", lay), ("dispatch", dis), ("combine", com))}
         ab = algorithmic_bytes(w)
@@ -571,6 +574,7 @@ def measure_decode(ep, dev, reps=10):
             "T": w.T, "H": w.H, "E": w.E, "K": w.K, "cap": w.cap, "quant": w.quant,
             "step_us_graph": round(step_us, 2),
             "tokens_per_s": round(w.T / (step_us * 1e-6), 1),
+            "step_us_graph_layout_dispatch_fused": round(fused_us, 2),
             "l2_flushed_us": {k: round(v, 2) for k, v in cold.items()},
             "dispatch_GBps_flushed": round(ab["dispatch"] / (cold["dispatch"] * 1e-6) / 1e9, 1),
             "combine_GBps_flushed": round(ab["combine"] / (cold["combine"] * 1e-6) / 1e9, 1),

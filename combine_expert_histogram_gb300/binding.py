@@ -54,7 +54,8 @@ _lib = None
 
 EXPORTS = ("ep_status_str", "ep_rows_capacity", "ep_scale_cols", "ep_scale_words",
            "ep_layout_workspace_bytes",
-           "ep_layout", "ep_dispatch", "ep_combine", "ep_masked_repack", "ep_layout_noalloc",
+           "ep_layout", "ep_dispatch", "ep_layout_dispatch", "ep_combine", "ep_masked_repack",
+           "ep_layout_noalloc",
            "ep_rank_layout", "ep_rank_expand", "ep_route_topk")
 NOALLOC_SCRATCH_BYTES = 256 * 1024
 
@@ -84,6 +85,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ep_layout.argtypes = [P, LP, P, SZ, P]
     L.ep_dispatch.restype = ctypes.c_int
     L.ep_dispatch.argtypes = [LP, P, I32, ctypes.c_int, P, P, P, P, P]
+    L.ep_layout_dispatch.restype = ctypes.c_int
+    L.ep_layout_dispatch.argtypes = [P, LP, P, SZ, P, I32, ctypes.c_int, P, P, P, P, P]
     L.ep_combine.restype = ctypes.c_int
     L.ep_combine.argtypes = [LP, P, I32, P, P, P]
     L.ep_masked_repack.restype = ctypes.c_int
@@ -292,6 +295,39 @@ def ep_dispatch(layout: Layout, x: torch.Tensor, quant: str = "none",
                                       _ptr(out_rows), _ptr(out_scales), _ptr(topk_w), _ptr(row_w),
                                       _stream(stream))
     _check(code, "ep_dispatch")
+    return out_rows, out_scales, row_w
+
+
+def ep_layout_dispatch(topk_idx: torch.Tensor, layout: Layout, x: torch.Tensor,
+                       quant: str = "none", out_rows: Optional[torch.Tensor] = None,
+                       out_scales: Optional[torch.Tensor] = None,
+                       topk_w: Optional[torch.Tensor] = None, row_w: Optional[torch.Tensor] = None,
+                       stream=None):
+    """ep_layout into ``layout`` and ep_dispatch of x, in one call (one kernel for
+    decode-sized batches).  Returns (out_rows, out_scales, row_w) like ep_dispatch."""
+    if topk_idx.dtype != torch.int32 or topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be int32 [T, K]")
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bf16")
+    T, K = topk_idx.shape
+    if (layout.num_tokens, layout.num_topk) != (T, K):
+        raise ValueError("layout shape does not match topk_idx")
+    H = x.shape[1]
+    rows = layout.rows_capacity
+    dev = x.device
+    if out_rows is None:
+        out_rows = torch.empty((max(rows, 1), H), device=dev,
+                               dtype=torch.bfloat16 if quant == "none" else torch.uint8)
+    if quant != "none" and out_scales is None:
+        out_scales = scale_buffer(layout, H, quant, device=dev)
+    if topk_w is not None and row_w is None:
+        row_w = torch.empty(max(rows, 1), device=dev, dtype=torch.float32)
+    ws = layout.workspace
+    code = load_library().ep_layout_dispatch(
+        _ptr(topk_idx) if T * K else None, ctypes.byref(layout.struct()), _ptr(ws),
+        ws.numel() * 4 if ws is not None else 0, _ptr(x), H, QUANT[quant], _ptr(out_rows),
+        _ptr(out_scales), _ptr(topk_w), _ptr(row_w), _stream(stream))
+    _check(code, "ep_layout_dispatch")
     return out_rows, out_scales, row_w
 
 

@@ -152,6 +152,31 @@ ep_status_t ep_dispatch(const ep_layout_t *L, const void *x, int32_t hidden, ep_
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_layout_dispatch(const int32_t *topk_idx, const ep_layout_t *L, void *workspace,
+                               size_t workspace_bytes, const void *x, int32_t hidden,
+                               ep_quant_t quant, void *out_rows, void *out_scales,
+                               const float *topk_w, float *row_w, ep_stream_t stream) {
+    // the argument rules of ep_layout and of ep_dispatch together
+    ep_status_t st = check_layout(L);
+    if (st != EP_OK) return st;
+    if (L->num_tokens > 0 && (!topk_idx || !aligned(topk_idx, 4))) return EP_ERR_INVALID_ARG;
+    const LayoutPlan plan = layout_plan(*L);
+    if (plan.smem > 227 * 1024) return EP_ERR_UNSUPPORTED;
+    if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 4)))
+        return EP_ERR_INVALID_ARG;
+    st = check_hidden(hidden, quant);
+    if (st != EP_OK) return st;
+    if (L->num_tokens > 0) {
+        if ((topk_w == nullptr) != (row_w == nullptr)) return EP_ERR_INVALID_ARG;
+        if (!aligned(topk_w, 4) || !aligned(row_w, 4)) return EP_ERR_INVALID_ARG;
+        if (quant != EP_QUANT_NONE && (!out_scales || !aligned(out_scales, 4))) return EP_ERR_INVALID_ARG;
+        if (!x || !out_rows || !aligned(x, 16) || !aligned(out_rows, 16)) return EP_ERR_INVALID_ARG;
+    }
+    return from_cuda(launch_layout_dispatch(topk_idx, *L, static_cast<int32_t *>(workspace), x,
+                                            hidden, quant, out_rows, out_scales, topk_w, row_w,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 ep_status_t ep_combine(const ep_layout_t *L, const void *y, int32_t hidden, const float *topk_w,
                        void *out, ep_stream_t stream) {
     ep_status_t st = check_layout(L);

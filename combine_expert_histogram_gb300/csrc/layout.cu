@@ -99,35 +99,6 @@ __device__ __forceinline__ void load_chunk(const int32_t *__restrict__ idx, int 
     classify_chunk(c0, c1, E, nbits, c);
 }
 
-// Expert totals (and, when pre != nullptr, the entries before `start`) of
-// the first TK entries, by shared-memory atomics; loads are issued eight at a
-// time ahead of their atomics.  Returns 1 if this thread saw an id outside
-// [-1, E).
-template <int NT>
-__device__ __forceinline__ int count_all(const int32_t *__restrict__ idx, int TK, int E, int start,
-                                         int32_t *tot, int32_t *pre) {
-    constexpr int kBatchLoads = 8;
-    int bad = 0;
-    for (int i0 = threadIdx.x; i0 < TK; i0 += NT * kBatchLoads) {
-        int ev[kBatchLoads];
-#pragma unroll
-        for (int u = 0; u < kBatchLoads; ++u) {
-            const int i = i0 + u * NT;
-            ev[u] = i < TK ? __ldg(idx + i) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatchLoads; ++u) {
-            const int i = i0 + u * NT, e = ev[u];
-            if (e >= 0 && e < E) {
-                atomicAdd(&tot[e], 1);
-                if (pre && i < start) atomicAdd(&pre[e], 1);
-            } else if (e != -1 && i < TK) {
-                bad = 1;
-            }
-        }
-    }
-    return bad;
-}
 
 __device__ __forceinline__ int id_bits(int E) { return 32 - __clz(E); }  // E itself must fit
 

@@ -218,6 +218,23 @@ ep_status_t ep_dispatch(const ep_layout_t *layout, const void *x, int32_t hidden
                         const float *topk_w, float *row_w, ep_stream_t stream);
 
 /*
+ * ep_layout_dispatch -- ep_layout followed by ep_dispatch in one call: the
+ * dispatch that "infers the layout from topk_idx" itself ([PR-24443]
+ * "Motivation": V2 folds V1's separate dispatch-layout pre-pass into
+ * dispatch).  Arguments, outputs and errors are exactly those of the two
+ * calls (topk_idx, layout and workspace as for ep_layout; x, hidden, quant,
+ * out_rows, out_scales, topk_w, row_w as for ep_dispatch), and the results
+ * are bit-identical to them.  Up to 8192 entries (T*K) one kernel does both
+ * (no workspace is read then: each CTA recounts the entries itself); larger
+ * batches run the two steps back to back.
+ */
+ep_status_t ep_layout_dispatch(const int32_t *topk_idx, const ep_layout_t *layout,
+                               void *workspace, size_t workspace_bytes, const void *x,
+                               int32_t hidden, ep_quant_t quant, void *out_rows,
+                               void *out_scales, const float *topk_w, float *row_w,
+                               ep_stream_t stream);
+
+/*
  * ep_combine -- top-k weighted reduction back to token order ([VLLM-EP]
  * "weighted reduction in combine"; combine reuses the dispatch handle,
  * [PR-24443] "Motivation").  The reduction is applied exactly once.

@@ -1,0 +1,132 @@
+"""ep_layout_dispatch: the layout and the dispatch in one call must give
+bit-identical results to ep_layout followed by ep_dispatch, and match the
+oracle, for decode-sized batches (one kernel) and beyond (two steps)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from combine_expert_histogram_gb300 import binding as ep
+from tests import gpu_harness as gh
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+W = workloads.Workload
+CASES = [
+    workloads.CONFIGS["qwen3_30b_a3b_decode"],
+    workloads.CONFIGS["dsv3_decode"],
+    workloads.CONFIGS["tiny"],
+    W("fused_mx", T=300, H=2048, E=64, K=8, routing="softmax", layout="contig", quant="mxfp8",
+      align=32, R=4, seed=81),
+    W("fused_mn_masked", T=500, H=1024, E=40, K=6, routing="softmax", layout="masked",
+      quant="fp8_ue8m0_mn", cap=90, seed=82),   # capacity overflow
+    W("fused_f32_ragged", T=777, H=640, E=100, K=9, routing="softmax", layout="contig",
+      quant="fp8_f32", align=16, seed=83),
+    W("fused_bf16_big_h", T=40, H=16384, E=8, K=2, routing="softmax", layout="masked",
+      quant="none", cap=40, seed=84),
+    W("two_steps", T=2000, H=512, E=64, K=8, routing="softmax", layout="contig",
+      quant="fp8_ue8m0", align=128, seed=85),   # 16000 entries: ep_layout + ep_dispatch
+]
+
+
+def _alloc(w, L):
+    rows = L.rows_capacity
+    dev = torch.device("cuda")
+    if w.quant == "none":
+        rows_t = torch.full((max(rows, 1), w.H), gh.SENTINEL_BF16, dtype=torch.int16,
+                            device=dev).view(torch.bfloat16)
+    else:
+        rows_t = torch.full((max(rows, 1), w.H), gh.SENTINEL_U8, dtype=torch.uint8, device=dev)
+    sc = None if w.quant == "none" else ep.scale_buffer(L, w.H, w.quant)
+    if sc is not None:
+        sc.zero_()
+    row_w = torch.zeros(max(rows, 1), dtype=torch.float32, device=dev)
+    return rows_t, sc, row_w
+
+
+def _arrays(L):
+    used = int(L.expert_offset[-1].item())  # rows past offset[E] are never written
+    return dict(dst_row=L.dst_row.cpu(), count=L.expert_count.cpu(), offset=L.expert_offset.cpu(),
+                rank_rows=L.rank_rows.cpu(), status=L.status.cpu(),
+                row_src=None if L.row_src is None else L.row_src[:used].cpu())
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_fused_equals_two_calls_and_oracle(w):
+    case = gh.make_case(w)
+    idx = case["idx"].copy()
+    if w.name == "fused_f32_ragged":  # unrouted entries and a bad id too
+        idx[::7, 3] = -1
+        idx[5, 0] = w.E + 2
+    idx_d = torch.from_numpy(idx).cuda()
+    case["idx"], case["idx_d"] = idx, idx_d
+    # reference: the two calls
+    L1 = ep.new_layout(w.T, w.K, w.E, w.layout, align=w.align, capacity=w.cap, num_ranks=w.R)
+    r1, s1, rw1 = _alloc(w, L1)
+    ep.ep_layout(idx_d, w.E, out=L1)
+    ep.ep_dispatch(L1, case["x_d"], w.quant, out_rows=r1, out_scales=s1, topk_w=case["w_d"],
+                   row_w=rw1)
+    # one call
+    L2 = ep.new_layout(w.T, w.K, w.E, w.layout, align=w.align, capacity=w.cap, num_ranks=w.R)
+    r2, s2, rw2 = _alloc(w, L2)
+    ep.ep_layout_dispatch(idx_d, L2, case["x_d"], w.quant, out_rows=r2, out_scales=s2,
+                          topk_w=case["w_d"], row_w=rw2)
+    torch.cuda.synchronize()
+    a1, a2 = _arrays(L1), _arrays(L2)
+    for k in a1:
+        if a1[k] is not None:
+            assert torch.equal(a1[k], a2[k]), f"layout array {k} differs"
+    assert torch.equal(r1.view(torch.uint8), r2.view(torch.uint8)), "rows differ"
+    if s1 is not None:
+        assert torch.equal(s1.view(torch.int32), s2.view(torch.int32)), "scales differ"
+    assert torch.equal(rw1.view(torch.int32), rw2.view(torch.int32)), "row weights differ"
+    # and the oracle (layout, rows, scales, row weights)
+    res = dict(L=L2, rows=L2.rows_capacity, out_rows=r2, out_scales=s2, row_w=rw2)
+    ref = gh.check_layout(w, case, res)
+    if w.quant != "fp8_ue8m0_mn":  # the MN-major word order has its own test file
+        gh.check_dispatch(w, case, res, ref, sample_tokens=512)
+
+
+def test_fused_graph_replay():
+    """Captured once with combine in a CUDA graph, replayed on fresh inputs."""
+    w = workloads.CONFIGS["qwen3_30b_a3b_decode"]
+    dev = torch.device("cuda")
+    idx_s = torch.zeros((w.T, w.K), dtype=torch.int32, device=dev)
+    w_s = torch.zeros((w.T, w.K), dtype=torch.float32, device=dev)
+    x_s = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    L = ep.new_layout(w.T, w.K, w.E, w.layout, capacity=w.cap)
+    rows = L.rows_capacity
+    out_rows = torch.empty((rows, w.H), dtype=torch.uint8, device=dev)
+    out_sc = ep.scale_buffer(L, w.H, w.quant)
+    y = workloads.make_expert_outputs(rows, w.H, seed=5, device=dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream()
+
+    def step():
+        ep.ep_layout_dispatch(idx_s, L, x_s, w.quant, out_rows=out_rows, out_scales=out_sc,
+                              stream=s)
+        ep.ep_combine(L, y, w_s, out=out, stream=s)
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for seed in (31, 32):
+        wi = w.with_(seed=seed)
+        idx, wts, x = workloads.make_inputs(wi)
+        idx_s.copy_(torch.from_numpy(idx))
+        w_s.copy_(torch.from_numpy(wts))
+        x_s.copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        case = dict(idx=idx, w=wts, x=x)
+        res = dict(L=L, rows=rows, out_rows=out_rows, out_scales=out_sc, row_w=None, y=y, out=out)
+        ref = gh.check_layout(wi, case, res)
+        gh.check_dispatch(wi, case, res, ref, check_row_w=False)
+        assert gh.check_combine(wi, case, res, ref) == 1.0
