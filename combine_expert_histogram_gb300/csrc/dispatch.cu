@@ -422,6 +422,58 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
     }
 }
 
+// Slot j of token row xr into registers: 16 bf16 (two 16-byte loads) for the
+// FP8 modes, 8 bf16 for bf16.
+template <int Q>
+__device__ __forceinline__ void load_slot(const uint16_t *xr, int j, uint4 &a, uint4 &b) {
+    if (Q == EP_QUANT_NONE) {
+        a = ld_stream(xr + j * 8);
+    } else {
+        a = ld_stream(xr + j * 16);
+        b = ld_stream(xr + j * 16 + 8);
+    }
+}
+
+// Dispatch token t from registers: thread i owns slots i, i + blockDim.x, ...
+// (whole warps step through the passes, lanes past the last slot idle along);
+// the first slot's data is in a0 / b0, or already quantised in q0 / sc0 when
+// `done0`; lanes k < K hold destination k in `cd`.  Every lane stores its 16
+// bytes to each destination row, and the scale words go out from registers.
+template <int Q>
+__device__ __forceinline__ void store_token(const uint16_t *x, int t, int H, int K, uint4 a0,
+                                            uint4 b0, bool done0, uint4 q0, uint32_t sc0, int cd,
+                                            uint8_t *out, uint32_t *scales, int mn_stride,
+                                            int mn_cap) {
+    constexpr bool kFp8 = Q != EP_QUANT_NONE;
+    constexpr bool kUe8m0 = Q == EP_QUANT_FP8_UE8M0 || Q == EP_QUANT_FP8_UE8M0_MN;
+    const int lane = threadIdx.x & 31;
+    const int G = H >> 7;
+    const int row_bytes = kFp8 ? H : 2 * H;
+    const int slots = kFp8 ? G * 8 : H / 8;
+    const int words = kUe8m0 ? (G + 3) >> 2 : G;
+    for (int j = threadIdx.x; j - lane < slots; j += blockDim.x) {
+        const bool act = j < slots;
+        const bool first = j == (int)threadIdx.x;
+        uint4 q = q0;
+        uint32_t sc = sc0;
+        if (!(first && done0)) {
+            uint4 a = a0, b = b0;
+            if (!first) {  // passes beyond the first: loaded here
+                a = b = make_uint4(0, 0, 0, 0);
+                if (act) load_slot<Q>(x + (size_t)t * H, j, a, b);
+            }
+            q = a;
+            if constexpr (kFp8) q = quant_slot<Q>(a, b, lane, sc);
+        }
+        for (int k = 0; k < K; ++k) {  // 16 bytes per lane to each destination
+            const int d = __shfl_sync(kFullMask, cd, k);
+            if (act && d >= 0) st_v4(out + (size_t)d * row_bytes + (size_t)j * 16, q);
+        }
+        if constexpr (kFp8)
+            store_scales<Q>(scales, sc, j, lane, slots, cd, K, G, words, mn_stride, mn_cap);
+    }
+}
+
 // Few tokens per SM: CTA c takes tokens c, c + gridDim.x, ...; thread i owns
 // slots i, i + blockDim.x, ... (whole warps step through the passes, lanes
 // past the last slot idle along) and keeps them in registers.
@@ -431,29 +483,14 @@ __global__ void __launch_bounds__(512)
                   uint8_t *__restrict__ out, uint32_t *__restrict__ scales, const float *topk_w,
                   float *__restrict__ row_w, int mn_stride, int mn_cap) {
     constexpr bool kFp8 = Q != EP_QUANT_NONE;
-    constexpr bool kUe8m0 = Q == EP_QUANT_FP8_UE8M0 || Q == EP_QUANT_FP8_UE8M0_MN;
     const int lane = threadIdx.x & 31;
-    const int G = H >> 7;
-    const int row_bytes = kFp8 ? H : 2 * H;
-    const int slots = kFp8 ? G * 8 : H / 8;
-    const int words = kUe8m0 ? (G + 3) >> 2 : G;
+    const int slots = kFp8 ? (H >> 7) * 8 : H / 8;
     const int step = gridDim.x;
     const bool weights = row_w != nullptr && threadIdx.x < K;
     const int n = cta_tokens(T, step);
-    // slot j of token tok: 16 bf16 (two 16-byte loads) for FP8, 8 for bf16
-    auto load = [&](int tok, int j, uint4 &a, uint4 &b) {
-        const uint16_t *xr = x + (size_t)tok * H;
-        if (kFp8) {
-            a = ld_stream(xr + j * 16);
-            b = ld_stream(xr + j * 16 + 8);
-        } else {
-            a = ld_stream(xr + j * 8);
-        }
-    };
-
     uint4 ca = make_uint4(0, 0, 0, 0), cb = ca, na = ca, nb = ca;
     const bool first_slot = (int)threadIdx.x < slots;
-    if (n > 0 && first_slot) load(blockIdx.x, threadIdx.x, ca, cb);
+    if (n > 0 && first_slot) load_slot<Q>(x + (size_t)blockIdx.x * H, threadIdx.x, ca, cb);
     // x was complete before the layout started: the first token's first slot
     // is quantised while the layout may still run; dst_row is the layout's
     // output (the wait is a no-op without a programmatic edge)
@@ -464,43 +501,32 @@ __global__ void __launch_bounds__(512)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int cd = n > 0 && lane < K ? ld_dep(dst_row + (size_t)blockIdx.x * K + lane) : -1;
     float cw = n > 0 && weights ? ld_dep(topk_w + (size_t)blockIdx.x * K + lane) : 0.0f;
-    for (int i = 0; i < n; ++i) {
+    // token i: the next token's slot and destinations go out first; token 0's
+    // first slot was quantised before the wait (a separate copy of the step,
+    // so that q0 / sc0 are dead for the others)
+    auto token = [&](int i, bool first) {
         const int t = blockIdx.x + i * step;
         int nd = -1;
         float nw = 0.0f;
-        if (i + 1 < n) {  // the next token, in flight meanwhile
-            if (first_slot) load(t + step, threadIdx.x, na, nb);
+        if (i + 1 < n) {
+            if (first_slot) load_slot<Q>(x + (size_t)(t + step) * H, threadIdx.x, na, nb);
             if (lane < K) {
                 nd = ld_dep(dst_row + (size_t)(t + step) * K + lane);
                 if (weights) nw = ld_dep(topk_w + (size_t)(t + step) * K + lane);
             }
         }
-        for (int j = threadIdx.x; j - lane < slots; j += blockDim.x) {
-            const bool act = j < slots;
-            uint4 q = q0;
-            uint32_t sc = sc0;
-            if (i > 0 || j != (int)threadIdx.x) {  // (token 0's first slot is done)
-                uint4 a = ca, b = cb;
-                if (j != (int)threadIdx.x) {  // passes beyond the first: loaded here
-                    a = b = make_uint4(0, 0, 0, 0);
-                    if (act) load(t, j, a, b);
-                }
-                q = a;
-                if constexpr (kFp8) q = quant_slot<Q>(a, b, lane, sc);
-            }
-            for (int k = 0; k < K; ++k) {  // 16 bytes per lane to each destination
-                const int d = __shfl_sync(kFullMask, cd, k);
-                if (act && d >= 0) st_v4(out + (size_t)d * row_bytes + (size_t)j * 16, q);
-            }
-            if constexpr (kFp8)
-                store_scales<Q>(scales, sc, j, lane, slots, cd, K, G, words, mn_stride, mn_cap);
-        }
+        if (first)
+            store_token<Q>(x, t, H, K, ca, cb, true, q0, sc0, cd, out, scales, mn_stride, mn_cap);
+        else
+            store_token<Q>(x, t, H, K, ca, cb, false, ca, 0, cd, out, scales, mn_stride, mn_cap);
         if (weights && cd >= 0) row_w[cd] = cw;
         ca = na;
         cb = nb;
         cd = nd;
         cw = nw;
-    }
+    };
+    if (n > 0) token(0, true);
+    for (int i = 1; i < n; ++i) token(i, false);
 }
 
 // ---- the layout and the dispatch of a decode-sized batch in one kernel ----
@@ -530,7 +556,6 @@ template <int Q>
 __global__ void __launch_bounds__(kFusedThreads) fused_kernel(FusedArgs f) {
     constexpr int NT = kFusedThreads, kWarps = NT / 32;
     constexpr bool kFp8 = Q != EP_QUANT_NONE;
-    constexpr bool kUe8m0 = Q == EP_QUANT_FP8_UE8M0 || Q == EP_QUANT_FP8_UE8M0_MN;
     extern __shared__ int32_t fsm[];
     const int E = f.E, K = f.K, H = f.H;
     int32_t *tot = fsm;           // [E] expert totals
@@ -541,25 +566,13 @@ __global__ void __launch_bounds__(kFusedThreads) fused_kernel(FusedArgs f) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t0 = blockIdx.x * f.per, t1 = min(f.T, t0 + f.per);
     const int i0 = t0 * K, i1 = t1 * K;
-    const int G = H >> 7;
-    const int row_bytes = kFp8 ? H : 2 * H;
-    const int slots = kFp8 ? G * 8 : H / 8;
-    const int words = kUe8m0 ? (G + 3) >> 2 : G;
-    auto load = [&](int tok, int j, uint4 &a, uint4 &b) {
-        const uint16_t *xr = f.x + (size_t)tok * H;
-        if (kFp8) {
-            a = ld_stream(xr + j * 16);
-            b = ld_stream(xr + j * 16 + 8);
-        } else {
-            a = ld_stream(xr + j * 8);
-        }
-    };
+    const int slots = kFp8 ? (H >> 7) * 8 : H / 8;
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the first token's slot is in flight during the layout work below
     uint4 ca = make_uint4(0, 0, 0, 0), cb = ca, na = ca, nb = ca;
     const bool first_slot = (int)threadIdx.x < slots;
-    if (t0 < t1 && first_slot) load(t0, threadIdx.x, ca, cb);
+    if (t0 < t1 && first_slot) load_slot<Q>(f.x + (size_t)t0 * H, threadIdx.x, ca, cb);
 
     // 1. expert totals and the entries before this CTA's tokens
     for (int e = threadIdx.x; e < E; e += NT) tot[e] = run[e] = 0;
@@ -636,27 +649,12 @@ __global__ void __launch_bounds__(kFusedThreads) fused_kernel(FusedArgs f) {
         int nd = -1;
         float nw = 0.0f;
         if (t + 1 < t1) {  // the next token, in flight meanwhile
-            if (first_slot) load(t + 1, threadIdx.x, na, nb);
+            if (first_slot) load_slot<Q>(f.x + (size_t)(t + 1) * H, threadIdx.x, na, nb);
             if (lane < K) nd = sdst[(t + 1 - t0) * K + lane];
             if (weights) nw = __ldg(f.topk_w + (size_t)(t + 1) * K + lane);
         }
-        for (int j = threadIdx.x; j - lane < slots; j += blockDim.x) {
-            const bool act = j < slots;
-            uint4 a = ca, b = cb;
-            if (j != (int)threadIdx.x) {  // passes beyond the first: loaded here
-                a = b = make_uint4(0, 0, 0, 0);
-                if (act) load(t, j, a, b);
-            }
-            uint4 q = a;
-            uint32_t sc = 0;
-            if constexpr (kFp8) q = quant_slot<Q>(a, b, lane, sc);
-            for (int k = 0; k < K; ++k) {
-                const int d = __shfl_sync(kFullMask, cd, k);
-                if (act && d >= 0) st_v4(f.out + (size_t)d * row_bytes + (size_t)j * 16, q);
-            }
-            if constexpr (kFp8)
-                store_scales<Q>(f.scales, sc, j, lane, slots, cd, K, G, words, f.mn_stride, f.mn_cap);
-        }
+        store_token<Q>(f.x, t, H, K, ca, cb, false, ca, 0, cd, f.out, f.scales, f.mn_stride,
+                       f.mn_cap);
         if (weights && cd >= 0) f.row_w[cd] = cw;
         ca = na;
         cb = nb;
