@@ -11,9 +11,10 @@
 // was measured to contract the pair into a fused multiply-add (results then
 // differ from separate rounding in cancelling sums).
 //
-// HBM-bound gather: one lane owns 8 output elements (16 bytes) of one token;
-// a warp covers 256 consecutive elements, so each of its K row loads is 512
-// contiguous bytes.  The lane first issues all loads of a batch of 8 entries
+// HBM-bound gather: one lane owns 8 output elements (16 bytes) of one token
+// -- 16 elements with one 256-bit load per row when the batch fills the GPU
+// (combine32_kernel) --; a warp covers 256 (512) consecutive elements, so
+// each of its K row loads is 512 (1024) contiguous bytes.  The lane first issues all loads of a batch of 8 entries
 // (8 x 16 B in flight per lane), then reduces them in k order.  The token's
 // destinations and weights come as 16-byte loads where K allows.
 #include <cuda_bf16.h>
@@ -116,6 +117,86 @@ __global__ void __launch_bounds__(kThreads)
     st_v4(out + (size_t)t * H + j * 8, make_uint4(o[0], o[1], o[2], o[3]));
 }
 
+// 32-byte lanes: one lane owns 16 outputs and reads 32 bytes of each row with
+// one 256-bit load (evict-first in L2: every row is read once); batches of 4
+// rows keep 128 bytes in flight per lane.  Needs H % 16 == 0 and 32-byte
+// aligned y and out.
+constexpr int kBatch32 = 4;
+
+__device__ __forceinline__ void ld_row32(const void *p, uint32_t (&r)[8]) {
+    asm volatile("ld.global.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "l"(p)
+                 : "memory");
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads)
+    combine32_kernel(const uint16_t *y, int K, int H, long long n_chunks, const int32_t *dst_row,
+                     const float *topk_w, uint16_t *__restrict__ out) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long c = (long long)blockIdx.x * kThreads + threadIdx.x;
+    if (c >= n_chunks) return;
+    const int CH = H >> 4;  // 16-output chunks per token
+    const int t = (int)(c / CH);
+    const int j = (int)(c - (long long)t * CH);
+    const int32_t *drow = dst_row + (size_t)t * K;
+    const float *wrow = topk_w + (size_t)t * K;
+    uint64_t acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0;
+    for (int k0 = 0; k0 < K; k0 += kBatch32) {
+        int d[kBatch32];
+        float w[kBatch32];
+        if (kVec) {  // K % 4 == 0: one quad per batch
+            const uint4 dq = ld_dep_v4(drow + k0);
+            const uint4 wq = ld_dep_v4(wrow + k0);
+            d[0] = (int)dq.x, d[1] = (int)dq.y, d[2] = (int)dq.z, d[3] = (int)dq.w;
+            w[0] = __uint_as_float(wq.x), w[1] = __uint_as_float(wq.y);
+            w[2] = __uint_as_float(wq.z), w[3] = __uint_as_float(wq.w);
+        } else {
+#pragma unroll
+            for (int u = 0; u < kBatch32; ++u) {
+                const int k = k0 + u;
+                d[u] = k < K ? ld_dep(drow + k) : -1;
+                w[u] = k < K ? ld_dep(wrow + k) : 0.0f;
+            }
+        }
+        uint32_t v[kBatch32][8];
+#pragma unroll
+        for (int u = 0; u < kBatch32; ++u) {
+            if (d[u] >= 0) {
+                ld_row32(y + (size_t)d[u] * H + (size_t)j * 16, v[u]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[u][i] = 0;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch32; ++u) {
+            if (d[u] < 0) continue;
+            const uint64_t w2 = f32x2(w[u], w[u]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 m = split_f32x2(mul_f32x2(w2, f32x2(bf16_lo(v[u][i]), bf16_hi(v[u][i]))));
+                const float2 a = split_f32x2(acc[i]);
+                acc[i] = f32x2(__fadd_rn(a.x, m.x), __fadd_rn(a.y, m.y));
+            }
+        }
+    }
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float2 a = split_f32x2(acc[i]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(a.x, a.y);
+        o[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    uint16_t *op = out + (size_t)t * H + (size_t)j * 16;
+    st_v4(op, make_uint4(o[0], o[1], o[2], o[3]));
+    st_v4(op + 8, make_uint4(o[4], o[5], o[6], o[7]));
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const ep_layout_t &L, const void *y, int H, const float *topk_w,
@@ -126,6 +207,20 @@ cudaError_t launch_combine(const ep_layout_t &L, const void *y, int H, const flo
     const long long blocks = (n + kThreads - 1) / kThreads;
     const bool vec = K % 4 == 0 && reinterpret_cast<uintptr_t>(L.dst_row) % 16 == 0 &&
                      reinterpret_cast<uintptr_t>(topk_w) % 16 == 0;
+    // 32-byte lanes when there is enough work to fill the GPU with half the
+    // threads (at least four CTAs per SM); small decode batches keep the
+    // 16-byte lanes' wider grid
+    const long long n32 = (long long)T * (H / 16);
+    const long long b32 = (n32 + kThreads - 1) / kThreads;
+    if (H % 16 == 0 && b32 >= 4LL * sm_count() && reinterpret_cast<uintptr_t>(y) % 32 == 0 &&
+        reinterpret_cast<uintptr_t>(out) % 32 == 0) {
+        return vec ? launch_kernel(combine32_kernel<true>, (int)b32, kThreads, 0, stream, true,
+                                   static_cast<const uint16_t *>(y), K, H, n32, L.dst_row, topk_w,
+                                   static_cast<uint16_t *>(out))
+                   : launch_kernel(combine32_kernel<false>, (int)b32, kThreads, 0, stream, true,
+                                   static_cast<const uint16_t *>(y), K, H, n32, L.dst_row, topk_w,
+                                   static_cast<uint16_t *>(out));
+    }
     return vec ? launch_kernel(combine_kernel<true>, (int)blocks, kThreads, 0, stream, true,
                                static_cast<const uint16_t *>(y), K, H, n, L.dst_row, topk_w,
                                static_cast<uint16_t *>(out))

@@ -266,11 +266,12 @@ def test_combine_cancelling_sums_bit_exact(K):
     assert np.array_equal(gh.to_np_u16(out), expect)
 
 
-@pytest.mark.parametrize("shift", ["dst_row", "topk_w"])
+@pytest.mark.parametrize("shift", ["dst_row", "topk_w", "y"])
 def test_combine_index_arrays_not_16_byte_aligned(shift):
-    """K % 4 == 0 but one index array only 4-byte aligned: combine must take
-    the one-entry-at-a-time loads and still match the oracle bit for bit."""
-    w = workloads.Workload("align4", T=777, H=512, E=32, K=8, routing="softmax",
+    """K % 4 == 0 but one index array only 4-byte aligned (combine must take
+    the one-entry-at-a-time loads), or y only 16-byte aligned (the 16-byte
+    lanes instead of 256-bit loads): still the oracle's bits."""
+    w = workloads.Workload("align4", T=7777, H=512, E=32, K=8, routing="softmax",
                            layout="contig", quant="none", align=16, seed=23)
     case = gh.make_case(w)
     L = ep.ep_layout(case["idx_d"], w.E, kind="contig", align=w.align)
@@ -284,6 +285,11 @@ def test_combine_index_arrays_not_16_byte_aligned(shift):
         buf[1:].copy_(wts.view(-1))
         wts = buf[1:].view(wts.shape)
     y = workloads.make_expert_outputs(L.rows_capacity, w.H, seed=3, device="cuda")
+    if shift == "y":  # same values, 16 bytes past a 32-byte boundary
+        buf = torch.empty(y.numel() + 8, dtype=torch.bfloat16, device="cuda")
+        buf[8:].copy_(y.view(-1))
+        y = buf[8:].view(y.shape)
+        assert y.data_ptr() % 32 == 16
     out = ep.ep_combine(L, y, wts)
     torch.cuda.synchronize()
     ref = oracle.default().layout(case["idx"], w.E, "contig", align=w.align)
