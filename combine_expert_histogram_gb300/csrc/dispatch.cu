@@ -742,6 +742,22 @@ __global__ void __launch_bounds__(32)
     }
 }
 
+// Self-test of the bounded wait: a barrier that expects 16 bytes no copy will
+// ever deliver (nothing is issued, so nothing can land after the CTA exits);
+// the wait must give up after `limit` SM clocks and the kernel report it.
+__global__ void wait_selftest_kernel(int32_t *status, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 16;" ::"r"(smem_addr(&bar))
+                     : "memory");
+    }
+    __syncthreads();
+    const bool ok = mbar_wait(&bar, 0, nullptr, limit);
+    if (__syncthreads_or(!ok) && threadIdx.x == 0) raise_status(status, EP_ERR_TIMEOUT);
+}
+
 // x stages that fit `budget` bytes beside `fixed` ones, no more than the tokens
 // one CTA of two per SM would take, within [2, max_stages].
 int stage_count(int T, int xstage_bytes, int fixed, int budget, int max_stages) {
@@ -933,6 +949,15 @@ cudaError_t launch_layout_dispatch(const int32_t *topk_idx, const ep_layout_t &L
         default:
             return launch_fused<EP_QUANT_FP8_UE8M0>(topk_idx, L, x, H, out_rows, out_scales, topk_w, row_w, stream);
     }
+}
+
+}  // namespace ep
+
+namespace ep {
+
+cudaError_t launch_wait_selftest(int32_t *status, long long limit_clocks, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 64, 0, stream>>>(status, limit_clocks);
+    return cudaGetLastError();
 }
 
 }  // namespace ep

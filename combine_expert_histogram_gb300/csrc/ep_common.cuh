@@ -203,6 +203,8 @@ LayoutPlan layout_plan(const ep_layout_t &L);
 cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t *workspace,
                           cudaStream_t stream);
 
+// One CTA waiting on a barrier nothing completes, for at most limit_clocks.
+cudaError_t launch_wait_selftest(int32_t *status, long long limit_clocks, cudaStream_t stream);
 // ep_layout followed by ep_dispatch; one kernel for decode-sized batches.
 cudaError_t launch_layout_dispatch(const int32_t *topk_idx, const ep_layout_t &L,
                                    int32_t *workspace, const void *x, int H, ep_quant_t quant,

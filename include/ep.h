@@ -235,6 +235,16 @@ ep_status_t ep_layout_dispatch(const int32_t *topk_idx, const ep_layout_t *layou
                                ep_stream_t stream);
 
 /*
+ * ep_selftest_bounded_wait -- diagnostic with no counterpart in the pages:
+ * checks on this GPU that the bounded waits of the dispatch kernels give up
+ * instead of hanging.  One CTA waits on a shared-memory barrier that expects
+ * bytes no copy will deliver, for at most `limit_clocks` SM clocks
+ * (1 .. 2^31), then raises EP_ERR_TIMEOUT into the device word *status
+ * (caller-owned, 4-byte aligned; its previous value is kept if larger).
+ */
+ep_status_t ep_selftest_bounded_wait(int32_t *status, int64_t limit_clocks, ep_stream_t stream);
+
+/*
  * ep_combine -- top-k weighted reduction back to token order ([VLLM-EP]
  * "weighted reduction in combine"; combine reuses the dispatch handle,
  * [PR-24443] "Motivation").  The reduction is applied exactly once.

@@ -136,3 +136,22 @@ def test_masked_capacity_exact_boundary(cap):
         assert np.array_equal(got, ref["dst_row"])
         assert int((got[:, 0] < 0).sum()) == extra  # only the last token's expert-0 entry
         assert int(L.expert_count.cpu()[0]) == T
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """The dispatch kernels' mbarrier waits are bounded: a wait on a barrier
+    that nothing completes returns after its limit and raises EP_ERR_TIMEOUT
+    into the status word, and the context stays usable."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_selftest_bounded_wait(status, 1 << 20)  # about half a millisecond
+    torch.cuda.synchronize()
+    assert int(status.item()) == ep.EP_ERR_TIMEOUT
+    # the GPU still runs work afterwards
+    idx = torch.tensor([[0, 3], [1, 2], [3, 0]], dtype=torch.int32, device="cuda")
+    L = ep.ep_layout(idx, 4, align=4)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0
+    ref = oracle.default().layout(idx.cpu().numpy(), 4, "contig", align=4)
+    assert L.dst_row.cpu().tolist() == ref["dst_row"].ravel().tolist()
+    with pytest.raises(ep.EPError):
+        ep.ep_selftest_bounded_wait(status, 0)  # limits outside 1 .. 2^31 are refused
