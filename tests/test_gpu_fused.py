@@ -130,3 +130,55 @@ def test_fused_graph_replay():
         ref = gh.check_layout(wi, case, res)
         gh.check_dispatch(wi, case, res, ref, check_row_w=False)
         assert gh.check_combine(wi, case, res, ref) == 1.0
+
+
+QUANTS = ["none", "fp8_f32", "fp8_ue8m0", "mxfp8", "fp8_ue8m0_mn"]
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fused_fuzz_equals_two_calls(seed):
+    """Random decode-sized shapes (up to 8192 entries, so one kernel) with -1
+    ids, repeated experts and small masked capacities: every output array
+    equals ep_layout followed by ep_dispatch."""
+    rng = np.random.default_rng(500 + seed)
+    K = int(rng.integers(1, 33))
+    T = int(rng.integers(1, 8192 // K + 1))
+    E = int(rng.choice([1, 5, 16, 64, 128, 256, 361, 1024]))
+    K = min(K, max(E, 1)) if E < K else K
+    quant = QUANTS[seed % len(QUANTS)]
+    H = int(rng.choice([128, 256, 1024, 2048, 7168, 32768] if quant != "none"
+                       else [8, 264, 2048, 7168, 32768]))
+    if H * T > 64 * 1024 * 1024:  # keep the buffers small
+        T = max(1, 64 * 1024 * 1024 // H)
+    layout = "masked" if rng.random() < 0.5 else "contig"
+    cap = int(rng.integers(1, max(2, T * K // max(E, 1) * 2 + 2)))
+    align = int(rng.choice([1, 4, 32, 128]))
+    R = int(rng.choice([r for r in (1, 2, 4) if E % r == 0]))
+    w = W(f"ffuzz{seed}", T=T, H=H, E=E, K=K, routing="softmax", layout=layout, quant=quant,
+          align=align, cap=cap, R=R, seed=seed)
+    idx = rng.integers(-1, E, size=(T, K)).astype(np.int32)
+    wts = rng.random((T, K)).astype(np.float32)
+    x = workloads.make_x(w, rng)
+    idx_d = torch.from_numpy(idx).cuda()
+    w_d = torch.from_numpy(wts).cuda()
+    x_d = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    outs = []
+    for one_call in (False, True):
+        L = ep.new_layout(T, K, E, layout, align=align, capacity=cap, num_ranks=R)
+        r, s, rw = _alloc(w, L)
+        if one_call:
+            ep.ep_layout_dispatch(idx_d, L, x_d, quant, out_rows=r, out_scales=s, topk_w=w_d,
+                                  row_w=rw)
+        else:
+            ep.ep_layout(idx_d, E, out=L)
+            ep.ep_dispatch(L, x_d, quant, out_rows=r, out_scales=s, topk_w=w_d, row_w=rw)
+        torch.cuda.synchronize()
+        outs.append((_arrays(L), r, s, rw))
+    (a1, r1, s1, rw1), (a2, r2, s2, rw2) = outs
+    for k in a1:
+        if a1[k] is not None:
+            assert torch.equal(a1[k], a2[k]), f"layout array {k} differs"
+    assert torch.equal(r1.view(torch.uint8), r2.view(torch.uint8)), "rows differ"
+    if s1 is not None:
+        assert torch.equal(s1.view(torch.int32), s2.view(torch.int32)), "scales differ"
+    assert torch.equal(rw1.view(torch.int32), rw2.view(torch.int32)), "row weights differ"
