@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kThreads)
     // Launched as a programmatic dependent: wait for the previous kernel on
     // the stream (it may have produced y) before reading anything.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // whatever follows waits for this kernel itself: let it launch now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long c = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (c >= n_chunks) return;
     const int CH = H >> 3;
@@ -136,6 +138,8 @@ __global__ void __launch_bounds__(kThreads)
     combine32_kernel(const uint16_t *y, int K, int H, long long n_chunks, const int32_t *dst_row,
                      const float *topk_w, uint16_t *__restrict__ out) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // whatever follows waits for this kernel itself: let it launch now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long c = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (c >= n_chunks) return;
     const int CH = H >> 4;  // 16-output chunks per token

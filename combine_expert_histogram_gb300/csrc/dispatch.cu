@@ -261,6 +261,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
     const int n = cta_tokens(T, step);
     uint8_t *orows = smem + (size_t)stages * xstage_bytes;
     const volatile int *fail = &s_fail;
+    // the next kernel (combine) waits for this one itself: let it launch now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -488,6 +490,7 @@ __global__ void __launch_bounds__(512)
     const int step = gridDim.x;
     const bool weights = row_w != nullptr && threadIdx.x < K;
     const int n = cta_tokens(T, step);
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // see quant_kernel
     uint4 ca = make_uint4(0, 0, 0, 0), cb = ca, na = ca, nb = ca;
     const bool first_slot = (int)threadIdx.x < slots;
     if (n > 0 && first_slot) load_slot<Q>(x + (size_t)blockIdx.x * H, threadIdx.x, ca, cb);
@@ -568,6 +571,10 @@ __global__ void __launch_bounds__(kFusedThreads) fused_kernel(FusedArgs f) {
     const int i0 = t0 * K, i1 = t1 * K;
     const int slots = kFp8 ? (H >> 7) * 8 : H / 8;
 
+    // The previous kernel may have produced topk_idx and x, and may still read
+    // the layout arrays: wait for it before anything else (a no-op for the
+    // ordinary launch used now); then the next kernel may launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the first token's slot is in flight during the layout work below
     uint4 ca = make_uint4(0, 0, 0, 0), cb = ca, na = ca, nb = ca;
@@ -678,6 +685,7 @@ __global__ void __launch_bounds__(32)
     const int step = gridDim.x;
     const int n = cta_tokens(T, step);
     const bool weights = row_w != nullptr && lane < K;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // see quant_kernel
 
     if (lane == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -885,7 +893,9 @@ cudaError_t launch_fused(const int32_t *topk_idx, const ep_layout_t &L, const vo
     const size_t smem = sizeof(int32_t) * (3 * (size_t)f.E + 1 + (size_t)f.per * f.K);
     cudaError_t err = allow_dynamic_smem(fused_kernel<Q>, smem);
     if (err != cudaSuccess) return err;
-    // an ordinary launch: topk_idx and x come from earlier work on the stream
+    // an ordinary launch: launched early, its large CTAs would sit on the SMs
+    // in griddepcontrol.wait and take registers from the previous kernel
+    // (measured: a combine before it ran slower by more than the overlap won)
     return launch_kernel(fused_kernel<Q>, grid, kFusedThreads, smem, stream, false, f);
 }
 

@@ -110,7 +110,13 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __global__ void __launch_bounds__(kTileThreads)
     tile_hist_kernel(const int32_t *__restrict__ idx, int TK, int E, int tile,
                      int32_t *__restrict__ ws, int32_t *__restrict__ status) {
-    pdl_launch_dependents();  // the assign kernel may start its own loads now
+    // First kernel of the layout, launched as a programmatic dependent: wait
+    // for the previous kernel on the stream (it may have produced topk_idx,
+    // and it may still read this layout's arrays) before anything else, and
+    // only then let the assign kernel -- which reads topk_idx before its own
+    // wait -- and dispatch start.
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ int32_t hist[];  // [E]
     for (int e = threadIdx.x; e < E; e += kTileThreads) hist[e] = 0;
     __syncthreads();
@@ -134,6 +140,7 @@ struct AssignArgs {
     int passes;  // passes per tile
     int tile, tiles;
     int self_hist;      // tiles > 1 without the histogram kernel (see layout_plan)
+    int first;          // the layout's only kernel (no tile_hist_kernel before it)
     const int32_t *ws;  // [tiles][E]; unused when tiles == 1 or self_hist
     int32_t *dst_row, *row_src, *count, *offset, *rank_rows, *status;
 };
@@ -150,7 +157,10 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
     int32_t *pre = off + E + 1;               // [E] self_hist: entries before this tile
     __shared__ int32_t scan_tmp[kWarps];
 
-    pdl_launch_dependents();  // dispatch may start loading and quantising x now
+    // as the first kernel: wait for the previous kernel before anything else
+    // (see tile_hist_kernel); then dispatch may start loading and quantising x
+    if (a.first) pdl_wait();
+    pdl_launch_dependents();
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool assigns = blockIdx.x < a.tiles;
@@ -398,6 +408,7 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     a.tile = p.tile;
     a.tiles = p.tiles;
     a.self_hist = p.self_hist;
+    a.first = p.threads == kSmallThreads || p.self_hist;
     a.ws = workspace;
     a.dst_row = L.dst_row;
     a.row_src = L.row_src;
@@ -409,18 +420,18 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     if (p.threads == kSmallThreads) {
         err = allow_dynamic_smem(assign_kernel<kSmallThreads>, p.smem);
         if (err != cudaSuccess) return err;
-        // first kernel of the layout: an ordinary launch, ordered after all prior work
+        // the only kernel: programmatic, waiting for the previous kernel first
         return launch_kernel(assign_kernel<kSmallThreads>, p.grid, kSmallThreads, p.smem, stream,
-                             false, a);
+                             true, a);
     }
-    if (p.self_hist) {  // the only kernel: an ordinary launch
+    if (p.self_hist) {  // the only kernel: programmatic, waiting for the previous kernel first
         err = allow_dynamic_smem(assign_kernel<kTileThreads>, p.smem);
         if (err != cudaSuccess) return err;
         return launch_kernel(assign_kernel<kTileThreads>, p.grid, kTileThreads, p.smem, stream,
-                             false, a);
+                             true, a);
     }
     err = launch_kernel(tile_hist_kernel, p.tiles, kTileThreads, sizeof(int32_t) * E, stream,
-                        false, topk_idx, TK, E, p.tile, workspace, L.status);
+                        true, topk_idx, TK, E, p.tile, workspace, L.status);
     if (err != cudaSuccess) return err;
     err = allow_dynamic_smem(assign_kernel<kTileThreads>, p.smem);
     if (err != cudaSuccess) return err;

@@ -212,6 +212,13 @@ ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *layout, void *
  *              subnormal blocks); q = E4M3_rn_satfinite(x / X) (values between
  *              448 and 512 saturate); byte b%4 of int32 word b/4 = log2(X) + 127.
  * and the same bytes are written to every row dst_row[t*K+k] >= 0.
+ *
+ * Ordering: the kernels are programmatic dependents of the previous work on
+ * the stream.  Dispatch reads x before it waits for its predecessor (to
+ * overlap the layout), so x must be complete when that predecessor started:
+ * always the case directly after ep_layout (whose first kernel waits for all
+ * earlier work); a kernel that writes x and triggers its dependents early
+ * (griddepcontrol.launch_dependents) must not run directly before ep_dispatch.
  */
 ep_status_t ep_dispatch(const ep_layout_t *layout, const void *x, int32_t hidden,
                         ep_quant_t quant, void *out_rows, void *out_scales,

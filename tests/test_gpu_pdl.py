@@ -1,10 +1,13 @@
 """Programmatic dependent launch: a kernel that starts while its predecessor
 still runs must read that predecessor's results only after waiting for it.
 
-Dispatch, combine, the layout's second kernel and the rank expand are launched
-as programmatic dependents.  Here the stream is first held behind a long fill,
-so that the library's launches queue back to back and every programmatic edge
-is live (dispatch starts while the layout runs, combine while dispatch runs).
+Every kernel of the library is launched as a programmatic dependent (the
+layout's first kernel and the one-call kernel wait for their predecessor
+before anything else), and dispatch and combine let their dependents launch
+at their start.  Here the stream is first held behind a long fill, so that the
+library's launches queue back to back and every programmatic edge is live
+(dispatch starts while the layout runs, combine while dispatch runs, the next
+step's layout while combine runs).
 The layout arrays and the outputs still hold an earlier call's results for
 other inputs -- valid-looking rows, not garbage -- so a read issued before its
 wait lands a row in the wrong place and the oracle check fails.
@@ -160,3 +163,46 @@ def test_rank_send_expand_queued():
     assert np.array_equal(out_rows.index_select(0, sel).cpu().numpy(), o_rows[valid])
     assert np.array_equal(out_sc.index_select(0, sel).cpu().numpy().view(np.uint32),
                           o_sc[valid].view(np.uint32))
+
+
+@pytest.mark.parametrize("w", [CASES[0], CASES[1], CASES[2], CASES[3]], ids=lambda w: w.name)
+def test_back_to_back_steps_share_layout_arrays(w):
+    """Two whole steps queued back to back on the same layout arrays: step A's
+    combine still reads dst_row while step B's layout is next in line to
+    rewrite it, and every kernel triggers its dependents early.  Each step must
+    match the oracle on its own inputs."""
+    dev = torch.device("cuda")
+    s = torch.cuda.Stream()
+    held = Held(s)
+    L = ep.new_layout(w.T, w.K, w.E, w.layout, align=w.align, capacity=w.cap, num_ranks=w.R)
+    rows = L.rows_capacity
+    y = workloads.make_expert_outputs(rows, w.H, seed=11, device=dev)
+    steps = []
+    for seed in (w.seed + 400, w.seed + 401):
+        idx, wts, x = workloads.make_inputs(w.with_(seed=seed))
+        steps.append(dict(
+            case=dict(idx=idx, w=wts, x=x),
+            idx_d=torch.from_numpy(idx).to(dev), w_d=torch.from_numpy(wts).to(dev),
+            x_d=torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16),
+            out_rows=torch.empty((rows, w.H), device=dev,
+                                 dtype=torch.bfloat16 if w.quant == "none" else torch.uint8),
+            out_scales=None if w.quant == "none" else ep.scale_buffer(L, w.H, w.quant),
+            out=torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)))
+    torch.cuda.synchronize()
+    held.hold()
+    with torch.cuda.stream(s):
+        for st in steps:
+            ep.ep_layout(st["idx_d"], w.E, out=L, stream=s)
+            ep.ep_dispatch(L, st["x_d"], w.quant, out_rows=st["out_rows"],
+                           out_scales=st["out_scales"], stream=s)
+            ep.ep_combine(L, y, st["w_d"], out=st["out"], stream=s)
+    torch.cuda.synchronize()
+    orc = oracle.default()
+    for st in steps:
+        ref = orc.layout(st["case"]["idx"], w.E, w.layout, align=w.align, cap=w.cap, R=w.R)
+        res = dict(out_rows=st["out_rows"], out_scales=st["out_scales"], row_w=None, y=y,
+                   out=st["out"])
+        gh.check_dispatch(w, st["case"], res, ref, check_row_w=False, check_empty=False)
+        assert gh.check_combine(w, st["case"], res, ref) == 1.0
+    # the arrays hold the second step's layout
+    assert gh.check_layout(w, steps[1]["case"], dict(L=L, rows=rows)) is not None
