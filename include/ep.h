@@ -38,7 +38,13 @@
  *   - All array arguments are DEVICE pointers owned by the caller; the library
  *     allocates nothing, keeps no global state and never synchronises the host.
  *     Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *     stream) and completes asynchronously.
+ *     stream) and completes asynchronously.  Kernels are launched as
+ *     programmatic dependents (programmatic dependent launch) and may start
+ *     while the previous kernel on the stream finishes; each waits for it
+ *     before touching its results, and the layout's first kernel before
+ *     anything else.  Dispatch and combine let the next kernel start early:
+ *     a caller's kernel launched as a programmatic dependent after them must
+ *     itself wait (griddepcontrol.wait) before reading their outputs.
  *   - Host-detectable errors (bad shapes, NULL or misaligned pointers, too many
  *     tokens) are returned synchronously and nothing is launched.  A failed
  *     launch returns EP_ERR_CUDA.
