@@ -1,10 +1,10 @@
 """Programmatic dependent launch: a kernel that starts while its predecessor
 still runs must read that predecessor's results only after waiting for it.
 
-Every kernel of the library is launched as a programmatic dependent (the
-layout's first kernel and the one-call kernel wait for their predecessor
-before anything else), and dispatch and combine let their dependents launch
-at their start.  Here the stream is first held behind a long fill, so that the
+The layout, dispatch, combine and rank kernels are launched as programmatic
+dependents (the layout's first kernel waits for its predecessor before
+anything else), and dispatch and combine let their dependents launch at their
+start; the one-call layout + dispatch kernel is an ordinary launch.  Here the stream is first held behind a long fill, so that the
 library's launches queue back to back and every programmatic edge is live
 (dispatch starts while the layout runs, combine while dispatch runs, the next
 step's layout while combine runs).
@@ -206,3 +206,67 @@ def test_back_to_back_steps_share_layout_arrays(w):
         assert gh.check_combine(w, st["case"], res, ref) == 1.0
     # the arrays hold the second step's layout
     assert gh.check_layout(w, steps[1]["case"], dict(L=L, rows=rows)) is not None
+
+
+def test_three_stream_pipeline_matches_synchronous():
+    """The end-to-end pattern: uploads on one stream, the three calls on a
+    second behind event waits, downloads on a third, two input sets in flight
+    alternately.  A programmatic launch on the compute stream must still wait
+    for the upload it depends on; every step must give the bytes a plain
+    synchronous run of the same inputs gives."""
+    w = CASES[3].with_(T=2048)
+    dev = torch.device("cuda")
+    hosts = []
+    for seed in (w.seed + 500, w.seed + 501):
+        idx, wts, x = workloads.make_inputs(w.with_(seed=seed))
+        hosts.append(dict(idx=torch.from_numpy(idx).pin_memory(),
+                          w=torch.from_numpy(wts).pin_memory(),
+                          x=torch.from_numpy(x.view(np.int16)).pin_memory()))
+    L = ep.new_layout(w.T, w.K, w.E, w.layout, align=w.align)
+    rows = L.rows_capacity
+    y = workloads.make_expert_outputs(rows, w.H, seed=13, device=dev)
+    out_rows = torch.empty((rows, w.H), dtype=torch.uint8, device=dev)
+    sc = ep.scale_buffer(L, w.H, w.quant)
+    ref = []
+    for h in hosts:
+        ep.ep_layout(h["idx"].to(dev), w.E, out=L)
+        ep.ep_dispatch(L, h["x"].to(dev).view(torch.bfloat16), w.quant, out_rows=out_rows,
+                       out_scales=sc)
+        ref.append(ep.ep_combine(L, y, h["w"].to(dev)).view(torch.int16).cpu())
+    torch.cuda.synchronize()
+    up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    bufs = [dict(idx=torch.empty((w.T, w.K), dtype=torch.int32, device=dev),
+                 w=torch.empty((w.T, w.K), dtype=torch.float32, device=dev),
+                 x=torch.empty((w.T, w.H), dtype=torch.int16, device=dev),
+                 out=torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev))
+            for _ in range(2)]
+    n = 8
+    got = [torch.empty((w.T, w.H), dtype=torch.int16).pin_memory() for _ in range(n)]
+    done, fetched = {}, {}
+    for i in range(n):
+        b, h = bufs[i % 2], hosts[i % 2]
+        if i >= 2:
+            up.wait_event(done[i - 2])       # the buffer's previous step has read it
+        with torch.cuda.stream(up):
+            for k in ("idx", "w", "x"):
+                b[k].copy_(h[k], non_blocking=True)
+            loaded = torch.cuda.Event()
+            loaded.record(up)
+        comp.wait_event(loaded)
+        if i >= 2:
+            comp.wait_event(fetched[i - 2])  # its previous output has been read back
+        with torch.cuda.stream(comp):
+            ep.ep_layout(b["idx"], w.E, out=L, stream=comp)
+            ep.ep_dispatch(L, b["x"].view(torch.bfloat16), w.quant, out_rows=out_rows,
+                           out_scales=sc, stream=comp)
+            ep.ep_combine(L, y, b["w"], out=b["out"], stream=comp)
+            done[i] = torch.cuda.Event()
+            done[i].record(comp)
+        down.wait_event(done[i])
+        with torch.cuda.stream(down):
+            got[i].copy_(b["out"].view(torch.int16), non_blocking=True)
+            fetched[i] = torch.cuda.Event()
+            fetched[i].record(down)
+    torch.cuda.synchronize()
+    bad = [i for i in range(n) if not torch.equal(got[i], ref[i % 2])]
+    assert not bad, f"pipelined steps {bad} differ from the synchronous run"
