@@ -182,3 +182,28 @@ def test_fused_fuzz_equals_two_calls(seed):
     if s1 is not None:
         assert torch.equal(s1.view(torch.int32), s2.view(torch.int32)), "scales differ"
     assert torch.equal(rw1.view(torch.int32), rw2.view(torch.int32)), "row weights differ"
+
+
+@pytest.mark.parametrize("layout", ["contig", "masked"])
+def test_fused_zero_tokens(layout):
+    """No tokens: the layout arrays say so (zero counts, zero rank rows,
+    offsets of empty experts, status OK) and nothing else is written."""
+    E, K, H = 16, 4, 256
+    dev = torch.device("cuda")
+    L = ep.new_layout(0, K, E, layout, align=128, capacity=8, num_ranks=4)
+    w = W("zero", T=0, H=H, E=E, K=K, routing="softmax", layout=layout, quant="fp8_f32",
+          align=128, cap=8, R=4, seed=0)
+    r, s, rw = _alloc(w, L)
+    r_before = r.clone()
+    L.expert_count.fill_(7)
+    L.rank_rows.fill_(7)
+    L.status.fill_(5)
+    idx_d = torch.empty((0, K), dtype=torch.int32, device=dev)
+    x_d = torch.empty((0, H), dtype=torch.bfloat16, device=dev)
+    ep.ep_layout_dispatch(idx_d, L, x_d, "fp8_f32", out_rows=r, out_scales=s)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0
+    assert not L.expert_count.any() and not L.rank_rows.any()
+    want = [e * 8 for e in range(E + 1)] if layout == "masked" else [0] * (E + 1)
+    assert L.expert_offset.cpu().tolist() == want
+    assert torch.equal(r, r_before)
