@@ -62,9 +62,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // shared memory to global memory, tracked by the issuing thread's bulk group.
+// The destination rows are written once and not read again by this kernel, so
+// their L2 lines are marked evict-first (at the DeepSeek-V3 prefill shape this
+// measured 1-2 us faster; the same hint on the x loads made the step slower).
 __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-                 "r"(smem_addr(ssrc)), "r"(bytes)
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 ::"l"(gdst), "r"(smem_addr(ssrc)), "r"(bytes), "l"(policy)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
