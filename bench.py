@@ -484,11 +484,13 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
-def graph_time_us(fns, stream, reps=10, flush=None):
+def graph_time_us(fns, stream, reps=50, flush=None, trials=5):
     """GPU time of one pass of `fns` (callables launching on `stream`), from a
     CUDA graph holding `reps` passes back to back: no host launch overhead
-    enters.  With `flush` (a callable writing 2x L2), each pass starts from a
-    flushed L2 and a flush-only graph's time is subtracted."""
+    enters.  One untimed replay warms up, then the median over `trials` timed
+    replays is divided by `reps`.  With `flush` (a callable writing 2x L2),
+    each pass starts from a flushed L2 and a flush-only graph's time is
+    subtracted."""
     import torch
 
     def capture(body):
@@ -501,12 +503,15 @@ def graph_time_us(fns, stream, reps=10, flush=None):
     def run(g):
         g.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b.record(stream)
+        events = []
+        for _ in range(trials):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            events.append((a, b))
         torch.cuda.synchronize()
-        return a.elapsed_time(b) * 1e3 / reps
+        return float(np.median([a.elapsed_time(b) for a, b in events])) * 1e3 / reps
 
     def body():
         if flush is not None:
@@ -521,7 +526,7 @@ def graph_time_us(fns, stream, reps=10, flush=None):
     return t
 
 
-def measure_decode(ep, dev, reps=10):
+def measure_decode(ep, dev, reps=50):
     """Decode shapes (masked layouts), timed from CUDA graphs: the whole step
     back to back (warm L2), each kernel from a flushed L2, and the masked
     repack on its own."""
