@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -110,7 +111,7 @@ class ClockSampler:
         except Exception:
             sel = []
         self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
-                    "-lms", "50"]
+                    "-lms", "25"]
 
     def start(self):
         try:
@@ -131,7 +132,7 @@ class ClockSampler:
             out, _ = self.proc.communicate()
         self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self, t_start, t_end):
+    def summary(self, t_start, t_end, strict=False):
         rows = []
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
@@ -150,8 +151,10 @@ class ClockSampler:
             rows.append((ts, sm, smax, reasons))
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        inwin = [r for r in rows if t_start - 0.05 <= r[0] <= t_end + 0.05]
+        inwin = [r for r in rows if t_start - 0.025 <= r[0] <= t_end + 0.025]
         window = "timed"
+        if strict:
+            return {"samples": len(inwin)}
         if not inwin:
             inwin, window = rows, "warmup+timed"
         reasons = sorted({x for r in inwin for x in r[3]})
@@ -196,7 +199,8 @@ def aggregate_tokens_per_s(tokens_per_rank: int, steps: int, world: int, max_ela
 
 # ------------------------------------------------------------ CPU baseline
 def oracle_tokens_per_s(w, idx, wts, x, y_host, n_tokens):
-    """Run the oracle's layout + dispatch + combine on the first n_tokens tokens."""
+    """Run the oracle's layout + dispatch + combine on the first n_tokens tokens;
+    returns (tokens/s of the whole pass, seconds, seconds per part)."""
     import oracle
     orc = oracle.default()
     sub_idx = np.ascontiguousarray(idx[:n_tokens])
@@ -204,11 +208,25 @@ def oracle_tokens_per_s(w, idx, wts, x, y_host, n_tokens):
     sub_x = np.ascontiguousarray(x[:n_tokens])
     t0 = time.perf_counter()
     L = orc.layout(sub_idx, w.E, w.layout, align=w.align, cap=w.cap, R=w.R)
+    t1 = time.perf_counter()
     orc.dispatch(sub_x, L["dst_row"], L["rows"], w.quant)
+    t2 = time.perf_counter()
     need = max(L["rows"], 1)
     orc.combine(y_host[:need], sub_w, L["dst_row"], w.H)
-    dt = time.perf_counter() - t0
-    return n_tokens / dt, dt
+    t3 = time.perf_counter()
+    parts = {"layout": t1 - t0, "dispatch": t2 - t1, "combine": t3 - t2}
+    return n_tokens / (t3 - t0), t3 - t0, parts
+
+
+def part_rates(w, n_tokens, parts):
+    """tokens/s and GB/s of each oracle part on the GPU kernels' algorithmic
+    bytes per token (the same counts as the kernels' roofline)."""
+    per_tok = {k: v / w.T for k, v in algorithmic_bytes(w).items()}
+    out = {}
+    for k, dt in parts.items():
+        out[k] = {"s": round(dt, 4), "tokens_per_s": round(n_tokens / dt, 1),
+                  "GB/s": round(per_tok[k] * n_tokens / dt / 1e9, 3)}
+    return out
 
 
 def y_host_rows(w, rows):
@@ -220,14 +238,15 @@ def y_host_rows(w, rows):
 
 def cpu_baseline(w, idx, wts, x, target_s=10.0):
     y_host = y_host_rows(w, 256 * w.K + w.E * w.align)
-    rate, dt = oracle_tokens_per_s(w, idx, wts, x, y_host, 256)
+    rate, dt, _ = oracle_tokens_per_s(w, idx, wts, x, y_host, 256)
     n = int(min(w.T, max(256, rate * target_s)))
     if n > 256:
         y_host = y_host_rows(w, n * w.K + w.E * w.align)
-        rate, dt = oracle_tokens_per_s(w, idx, wts, x, y_host, n)
+    rate, dt, parts = oracle_tokens_per_s(w, idx, wts, x, y_host, n)
     return {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"first {n} of {w.T} tokens of {w.name}, one pass of layout + dispatch "
-                      f"+ combine, single-threaded C oracle ({dt:.1f} s)"}
+                      f"+ combine, single-threaded C oracle ({dt:.1f} s)",
+            **part_rates(w, n, parts)}
 
 
 def oracle_tokens_per_s_threads(w, idx, wts, x, y_host, n_tokens, threads):
@@ -250,6 +269,7 @@ def oracle_tokens_per_s_threads(w, idx, wts, x, y_host, n_tokens, threads):
     with ThreadPoolExecutor(threads) as pool:
         t0 = time.perf_counter()
         L = orc.layout(sub_idx, w.E, w.layout, align=w.align, cap=w.cap, R=w.R)
+        t1 = time.perf_counter()
         rows = max(L["rows"], 1)
         d = np.ascontiguousarray(L["dst_row"], dtype=np.int32)
         if w.quant == "none":
@@ -269,25 +289,32 @@ def oracle_tokens_per_s_threads(w, idx, wts, x, y_host, n_tokens, threads):
             lib.orc_combine(at(y_host, 0), at(sub_w, r[0] * K * 4), at(d, r[0] * K * 4),
                             r[1] - r[0], K, H, at(comb, r[0] * H * 2))
 
+        t2 = time.perf_counter()  # output buffers are allocated outside the parts
         list(pool.map(disp, ranges))
+        t3 = time.perf_counter()
         list(pool.map(combine, ranges))
-        dt = time.perf_counter() - t0
-    return n_tokens / dt, dt
+        t4 = time.perf_counter()
+    parts = {"layout": t1 - t0, "dispatch": t3 - t2, "combine": t4 - t3}
+    total = sum(parts.values())
+    return n_tokens / total, total, parts
 
 
 def cpu_baseline_threads(w, idx, wts, x, reps=3):
-    """Token-parallel oracle on every host core: median of `reps` runs."""
+    """Token-parallel oracle on every host core: median of `reps` runs (whole
+    pass), each part's median reported beside it."""
     threads = os.cpu_count() or 1
     n = w.T
     y_host = y_host_rows(w, n * w.K + w.E * w.align)
-    runs = sorted(oracle_tokens_per_s_threads(w, idx, wts, x, y_host, n, threads)
-                  for _ in range(reps))
-    rate, dt = runs[len(runs) // 2]
+    runs = [oracle_tokens_per_s_threads(w, idx, wts, x, y_host, n, threads) for _ in range(reps)]
+    rate, dt, _ = sorted(runs, key=lambda r: r[1])[len(runs) // 2]
+    parts = {k: float(np.median([r[2][k] for r in runs])) for k in ("layout", "dispatch",
+                                                                      "combine")}
     return {"value": rate, "unit": "tokens/s", "cores": threads,
             "kind": "oracle, token-parallel",
             "sample": f"all {n} tokens of {w.name}: layout on one thread, dispatch and combine "
                       f"on {threads} threads over disjoint token ranges; median of {reps} "
-                      f"({dt:.2f} s)"}
+                      f"({dt:.2f} s)",
+            **part_rates(w, n, parts)}
 
 
 # ---------------------------------------------------------------- reference
@@ -297,16 +324,19 @@ def run_reference(args, w):
         return
     idx, wts, x = workloads.make_inputs(w)
     y_host = y_host_rows(w, 256 * w.K + w.E * w.align)
-    rate, _ = oracle_tokens_per_s(w, idx, wts, x, y_host, 256)
+    rate, _, _ = oracle_tokens_per_s(w, idx, wts, x, y_host, 256)
     budget = 60.0  # seconds for the whole --warmup + --steps run
     n = int(max(16, min(w.T, rate * budget / max(1, args.steps + args.warmup))))
     y_host = y_host_rows(w, n * w.K + w.E * w.align)
     for _ in range(args.warmup):
         oracle_tokens_per_s(w, idx, wts, x, y_host, n)
     total_dt = 0.0
+    part_dt = {"layout": 0.0, "dispatch": 0.0, "combine": 0.0}
     for _ in range(args.steps):
-        _, dt = oracle_tokens_per_s(w, idx, wts, x, y_host, n)
+        _, dt, parts = oracle_tokens_per_s(w, idx, wts, x, y_host, n)
         total_dt += dt
+        for k in part_dt:
+            part_dt[k] += parts[k]
     value = n * args.steps / total_dt
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -316,7 +346,8 @@ def run_reference(args, w):
             "config": bench_config(w, 1),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": f"first {n} of {w.T} tokens per step, one pass of "
-                                       "layout + dispatch + combine, single-threaded C oracle"},
+                                       "layout + dispatch + combine, single-threaded C oracle",
+                             **part_rates(w, n * args.steps, part_dt)},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -386,40 +417,55 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     L.check_status()
 
-    # Per-kernel events go on every --event-every'th step only: an event
-    # between two kernels also cuts the programmatic (overlapped) launch of
-    # the next one, so the other steps run exactly as a caller would run them.
-    every = max(1, args.event_every)
-    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-           for i in range(0, args.steps, every)}
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    # The timed steps carry no event between kernels: an event there would
+    # also cut the programmatic (overlapped) launch of the next kernel, so the
+    # steps run exactly as a caller would run them.
     start.record(stream)
-    for i in range(args.steps):
-        step(evs.get(i))
+    for _ in range(args.steps):
+        step()
     end.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), dev if world > 1 else None)
+
+    # Per-kernel times, independent of --steps: further steps with an event
+    # between every two kernels (each kernel then starts only after the one
+    # before it has finished), at least --kernel-reps of them and at least
+    # --kernel-seconds of GPU time, median per kernel.  The clock sampler keeps
+    # running through these steps, so the clock record covers more than the
+    # (possibly short) timed region.
+    kreps = max(args.kernel_reps, int(math.ceil(args.kernel_seconds * 1e3 * args.steps
+                                                 / max(elapsed_ms, 1e-3))))
+    kreps = min(kreps, 20000)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(kreps)]
+    with torch.cuda.stream(stream):
+        for e in evs:
+            step(e)
+    torch.cuda.synchronize()
+    t_wall2 = time.time()
     if sampler:
         time.sleep(0.15)
         sampler.stop()
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), dev if world > 1 else None)
-
     seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
-                    for e in evs.values()])
-    lay_ms, disp_ms, comb_ms = seg.mean(axis=0)
+                    for e in evs])
     ab = algorithmic_bytes(w)
     peak, peak_src = peak_hbm()
     kern = {}
-    for name, ms in (("layout", lay_ms), ("dispatch", disp_ms), ("combine", comb_ms)):
+    for j, name in enumerate(("layout", "dispatch", "combine")):
+        ms = float(np.median(seg[:, j]))
         gbs = ab[name] / (ms * 1e-3) / 1e9
-        kern[name] = {"us": round(ms * 1e3, 2), "algorithmic_bytes": ab[name],
+        kern[name] = {"us": round(ms * 1e3, 2), "us_mean": round(float(seg[:, j].mean()) * 1e3, 2),
+                      "us_p10_p90": [round(float(np.percentile(seg[:, j], q)) * 1e3, 2)
+                                     for q in (10, 90)],
+                      "launches": int(kreps), "algorithmic_bytes": ab[name],
                       "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
 
     # end to end through the public API with pinned host buffers
@@ -452,7 +498,8 @@ def run_ours(args, w):
         "config": bench_config(w, world),
         "step_gbs": round(sum(ab.values()) * args.steps * world / (elapsed_ms * 1e-3) / 1e9, 1),
         "kernels": kern,
-        "kernel_events": f"per-kernel events on {len(evs)} of {args.steps} timed steps",
+        "kernel_events": (f"median over {kreps} further steps with an event between every two "
+                          "kernels (none in the timed steps)"),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
@@ -461,7 +508,10 @@ def run_ours(args, w):
         "gpu_launches": launches_per_step * args.steps,
     }
     if sampler:
-        line["clocks"] = sampler.summary(t_wall0, t_wall1)
+        # the timed steps and the per-kernel timing steps that follow them
+        line["clocks"] = sampler.summary(t_wall0, t_wall2)
+        line["clocks"]["window"] = "timed steps + per-kernel timing steps"
+        line["clocks"]["samples_timed_only"] = sampler.summary(t_wall0, t_wall1, strict=True)["samples"]
     if e2e:
         line["e2e"] = e2e
     sections = set(args.sections.split(",")) if args.sections else set()
@@ -475,6 +525,8 @@ def run_ours(args, w):
         line["rank_dedup"] = measure_rank_dedup(ep, dev)
     if "router" in sections:
         line["router"] = measure_router(ep, dev)
+    if "skewed" in sections:
+        line["skewed_zipf"] = measure_skewed(ep, dev, peak)
     line["context"] = PAGES_CONTEXT
     if not args.skip_cpu and world == 1:  # the CPU baseline is an N=1 figure
         line["cpu_baseline"] = cpu_baseline(w, idx, wts, x)
@@ -588,6 +640,65 @@ def measure_decode(ep, dev, reps=50):
         }
         del y, out_rows, slab, rows_c
         torch.cuda.empty_cache()
+    return res
+
+
+def measure_skewed(ep, dev, peak, reps=100):
+    """The skewed-load workload (T=8192, H=4096, E=128, top-8 Zipf(1.2) experts,
+    Dirichlet weights; 8 logical ranks of 16 experts; bf16 rows): layout,
+    dispatch and combine each timed with CUDA events in steps of the three
+    calls (an event between every two kernels), median over `reps` steps.
+    Between two steps the combine streams 0.6 GB through L2, which evicts the
+    67 MB of x that the next dispatch reads."""
+    import torch
+    w = workloads.CONFIGS["skewed_zipf"]
+    idx, wts, x = workloads.make_inputs(w)
+    idx_d = torch.from_numpy(idx).to(dev)
+    w_d = torch.from_numpy(wts).to(dev)
+    x_d = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    L = ep.new_layout(w.T, w.K, w.E, w.layout, align=w.align, num_ranks=w.R, device=dev)
+    rows = L.rows_capacity
+    out_rows = torch.empty((rows, w.H), dtype=torch.bfloat16, device=dev)
+    y = workloads.make_expert_outputs(rows, w.H, seed=7, device=dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def step(e):
+        e[0].record(s)
+        ep.ep_layout(idx_d, w.E, out=L, stream=s)
+        e[1].record(s)
+        ep.ep_dispatch(L, x_d, w.quant, out_rows=out_rows, stream=s)
+        e[2].record(s)
+        ep.ep_combine(L, y, w_d, out=out, stream=s)
+        e[3].record(s)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps + 5)]
+    with torch.cuda.stream(s):
+        for e in evs:
+            step(e)
+    torch.cuda.synchronize()
+    L.check_status()
+    seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+                    for e in evs[5:]])
+    ab = algorithmic_bytes(w)
+    res = {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "K": w.K, "ranks": w.R,
+           "quant": "bf16 rows", "steps_timed": reps,
+           "algorithmic_bytes_per_token": {k: ab[k] // w.T for k in ("dispatch", "combine")}}
+    for j, name in enumerate(("layout", "dispatch", "combine")):
+        us = float(np.median(seg[:, j])) * 1e3
+        gbs = ab[name] / (us * 1e-6) / 1e9
+        res[name] = {"us": round(us, 2), "tokens_per_s": round(w.T / (us * 1e-6), 1),
+                     "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    rr = L.rank_rows.cpu().numpy().astype(int)
+    cnt = L.expert_count.cpu().numpy().astype(int)
+    off = L.expert_offset.cpu().numpy().astype(int)
+    per = w.E // w.R
+    res["rank_rows"] = rr.tolist()
+    res["rank_rows_padded"] = [int(off[(r + 1) * per] - off[r * per]) for r in range(w.R)]
+    res["hot_rank_share"] = round(float(rr.max() / max(rr.sum(), 1)), 4)
+    res["hottest_expert_rows"] = int(cnt.max())
+    del out_rows, y
+    torch.cuda.empty_cache()
     return res
 
 
@@ -779,14 +890,17 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer e2e leg")
-    ap.add_argument("--event-every", type=int, default=10,
-                    help="per-kernel CUDA events on every N-th timed step")
+    ap.add_argument("--kernel-reps", type=int, default=100,
+                    help="minimum number of per-kernel timing steps after the timed region")
+    ap.add_argument("--kernel-seconds", type=float, default=0.5,
+                    help="minimum GPU time of the per-kernel timing steps")
     ap.add_argument("--skip-decode", action="store_true",
                     help="omit every extra measurement section (same as --sections '')")
-    ap.add_argument("--sections", default="variants,decode,rank,router",
+    ap.add_argument("--sections", default="variants,decode,rank,router,skewed",
                     help="extra measurements after the timed steps: variants (dispatch in "
                          "every quantisation mode), decode (masked decode shapes), rank "
-                         "(per-rank deduplicated sending), router (ep_route_topk)")
+                         "(per-rank deduplicated sending), router (ep_route_topk), skewed "
+                         "(the Zipf-skewed bf16 workload's layout, dispatch and combine)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (small cases for profiling; not a bench line)")
     args = ap.parse_args()

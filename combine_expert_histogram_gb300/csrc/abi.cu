@@ -77,6 +77,15 @@ ep_status_t check_hidden(int32_t H, ep_quant_t quant) {
 ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 
 }  // namespace
+
+ep_status_t check_layout_call(const int32_t *topk_idx, const ep_layout_t *L) {
+    const ep_status_t st = check_layout(L);
+    if (st != EP_OK) return st;
+    if (L->num_tokens > 0 && (!topk_idx || !aligned(topk_idx, 4))) return EP_ERR_INVALID_ARG;
+    if (layout_plan(*L).smem > 227 * 1024) return EP_ERR_UNSUPPORTED;  // more entries than one CTA can rank
+    return EP_OK;
+}
+
 }  // namespace ep
 
 using namespace ep;
@@ -124,11 +133,9 @@ size_t ep_layout_workspace_bytes(const ep_layout_t *L) {
 
 ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *L, void *workspace,
                       size_t workspace_bytes, ep_stream_t stream) {
-    ep_status_t st = check_layout(L);
+    const ep_status_t st = check_layout_call(topk_idx, L);
     if (st != EP_OK) return st;
-    if (L->num_tokens > 0 && (!topk_idx || !aligned(topk_idx, 4))) return EP_ERR_INVALID_ARG;
     const LayoutPlan plan = layout_plan(*L);
-    if (plan.smem > 227 * 1024) return EP_ERR_UNSUPPORTED;  // more entries than one CTA can rank
     const size_t need = plan.ws_bytes;
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 4)))
         return EP_ERR_INVALID_ARG;

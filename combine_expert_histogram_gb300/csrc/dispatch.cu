@@ -31,7 +31,12 @@
 // Dispatch is launched as the layout's programmatic dependent: the first rows
 // load while the layout finishes, and destinations are read only after
 // griddepcontrol.wait.  Every mbarrier wait is bounded (about a second); on
-// expiry the kernel raises EP_ERR_TIMEOUT, lets its copies land and returns.
+// expiry the kernel raises EP_ERR_TIMEOUT, waits for the row copies it issued
+// to land and returns.  That drain is bounded as well (about a second in
+// all): a copy from ordinary global memory lands long before, but if the
+// drain itself ran out the CTA would exit with a copy into its shared memory
+// still pending, which is undefined; EP_ERR_TIMEOUT is then the only thing the
+// kernel guarantees, and the caller should treat the context as suspect.
 #include <cuda_fp8.h>
 
 #include "ep_common.cuh"

@@ -198,8 +198,12 @@ struct LayoutPlan {
     size_t ws_bytes;  // scratch: tiles x E int32 per-tile histograms (0 when tiles == 1
                       // or self_hist)
     bool self_hist;   // several tiles, one kernel: every CTA recounts all entries itself
+    bool cluster;     // decode-sized: one kernel of one thread-block cluster (tiles = its CTAs,
+                      // for the largest cluster; the launch may use fewer, larger slices)
 };
 LayoutPlan layout_plan(const ep_layout_t &L);
+// Every argument check of ep_layout except the workspace's, in its order.
+ep_status_t check_layout_call(const int32_t *topk_idx, const ep_layout_t *L);
 cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t *workspace,
                           cudaStream_t stream);
 

@@ -36,7 +36,11 @@
  *
  * Conventions for every call:
  *   - All array arguments are DEVICE pointers owned by the caller; the library
- *     allocates nothing, keeps no global state and never synchronises the host.
+ *     allocates no memory and never synchronises the host.  Its only state is
+ *     a per-device cache of the SM count (read once with
+ *     cudaDeviceGetAttribute) and, for ep_layout_noalloc alone, the fixed
+ *     device array that call uses as scratch (with its looked-up address);
+ *     every other entry point keeps nothing between calls.
  *     Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and completes asynchronously.  Kernels are launched as
  *     programmatic dependents (programmatic dependent launch) and may start
@@ -53,7 +57,10 @@
  *     out-of-bounds write): EP_ERR_BAD_EXPERT_ID for an id outside [-1, E),
  *     EP_ERR_CAPACITY for a masked expert receiving more than `capacity` rows,
  *     EP_ERR_TIMEOUT if a bulk copy a kernel waits for never completes (the
- *     wait is bounded; the kernel then drains its copies and returns).
+ *     wait is bounded; the kernel then waits, again for a bounded time, for
+ *     the copies it issued and returns; if even that drain runs out, a copy
+ *     may still be landing in a CTA that has exited, and the context should
+ *     be treated as suspect).
  *     Read it back after the stream completes.
  *   - bf16 means IEEE binary32's upper 16 bits; FP8 means E4M3FN (OCP OFP8).
  */
@@ -371,10 +378,14 @@ ep_status_t ep_rank_expand(const ep_layout_t *rank_layout, const ep_layout_t *la
  *
  *   Same arguments and results as ep_layout, minus the workspace.
  *   The array holds EP_NOALLOC_SCRATCH_BYTES on every GPU that loads the
- *   library, until the process exits.  A shape whose ep_layout_workspace_bytes()
- *   exceeds it is rejected with EP_ERR_CAPACITY before any launch.
+ *   library, until the process exits.  Arguments are checked first, exactly
+ *   as ep_layout checks them (same codes); then a shape whose
+ *   ep_layout_workspace_bytes() exceeds the array is rejected with
+ *   EP_ERR_CAPACITY, still before any launch.
  *   The first call on a device looks up the array's device address (with that
- *   device current); make it before any stream capture.  All calls share the
+ *   device current); make it before any stream capture.  The address is kept
+ *   per device and CUDA context: after cudaDeviceReset the next call looks it
+ *   up again in the new context (again before any capture).  All calls share the
  *   array: calls whose work overlaps on the GPU race and must be ordered by
  *   the caller (one stream, or events).  Nothing in the array needs clearing
  *   between calls.

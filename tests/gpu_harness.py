@@ -3,8 +3,9 @@
 Comparisons:
   * layout (counts, offsets, dst_row, row_src, rank_rows, status): bit-exact;
   * dispatched rows and scales (bf16, E4M3 bytes, fp32 / UE8M0 scales):
-    bit-exact on every valid row (or on every row of sampled tokens at full
-    size), and rows the layout leaves empty keep their sentinel bytes;
+    bit-exact on every valid row of every token (or of sampled tokens where a
+    caller asks for a sample), compared in token chunks, and rows the layout
+    leaves empty keep their sentinel bytes;
   * combine output: within 1 bf16 ulp (the two sides use the same summation
     order, so it is expected to be bit-exact; ``exact_fraction`` reports it).
 """
@@ -19,6 +20,9 @@ from combine_expert_histogram_gb300 import binding as ep
 
 SENTINEL_U8 = 0xA5
 SENTINEL_BF16 = -23131  # int16 view of 0xA5A5
+# tokens per oracle call when comparing dispatch and combine (bounds host memory:
+# 2048 tokens of the DeepSeek-V3 shape are 117 MB of E4M3 rows, 235 MB of y)
+CHUNK_TOKENS = 2048
 
 
 def to_np_u16(t: torch.Tensor) -> np.ndarray:
@@ -102,6 +106,27 @@ def check_dispatch(w, case, g, ref, sample_tokens=None, seed=0, orc=None, check_
     else:
         rng = np.random.default_rng(seed)
         toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, sample_tokens, replace=False)]))
+    # token chunks bound the host memory of the oracle's rows and the copies
+    for c0 in range(0, toks.size, CHUNK_TOKENS):
+        _check_dispatch_tokens(w, case, g, dst, toks[c0:c0 + CHUNK_TOKENS], orc, check_row_w)
+    if not check_empty:
+        return
+    # rows no entry maps to keep the sentinel (padding and empty slots)
+    rows = ref["rows"]
+    used = torch.zeros(max(rows, 1), dtype=torch.bool, device=g["out_rows"].device)
+    alld = torch.from_numpy(dst[dst >= 0].astype(np.int64)).to(used.device)
+    used[alld] = True
+    empty = ~used[:rows]
+    if empty.any():
+        buf = g["out_rows"][:rows][empty]
+        if w.quant == "none":
+            assert bool((buf.view(torch.int16) == SENTINEL_BF16).all())
+        else:
+            assert bool((buf == SENTINEL_U8).all())
+
+
+def _check_dispatch_tokens(w, case, g, dst, toks, orc, check_row_w):
+    """Rows, scales and row weights of tokens `toks`, bit for bit."""
     sub_dst = dst[toks]
     valid = sub_dst >= 0
     # oracle on the sampled tokens, written to compact rows 0..n-1
@@ -121,20 +146,6 @@ def check_dispatch(w, case, g, ref, sample_tokens=None, seed=0, orc=None, check_
     if check_row_w:
         assert np.array_equal(g["row_w"].index_select(0, sel).cpu().numpy().view(np.uint32),
                               o_w[osel].view(np.uint32))
-    if not check_empty:
-        return
-    # rows no entry maps to keep the sentinel (padding and empty slots)
-    rows = ref["rows"]
-    used = torch.zeros(max(rows, 1), dtype=torch.bool, device=g["out_rows"].device)
-    alld = torch.from_numpy(dst[dst >= 0].astype(np.int64)).to(used.device)
-    used[alld] = True
-    empty = ~used[:rows]
-    if empty.any():
-        buf = g["out_rows"][:rows][empty]
-        if w.quant == "none":
-            assert bool((buf.view(torch.int16) == SENTINEL_BF16).all())
-        else:
-            assert bool((buf == SENTINEL_U8).all())
 
 
 def check_combine(w, case, g, ref, sample_tokens=None, seed=0, orc=None):
@@ -149,13 +160,44 @@ def check_combine(w, case, g, ref, sample_tokens=None, seed=0, orc=None):
     else:
         rng = np.random.default_rng(seed + 1)
         toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, sample_tokens, replace=False)]))
-    sub = dst[toks]
-    flat = sub.ravel()
-    gather = torch.from_numpy(np.where(flat >= 0, flat, 0).astype(np.int64)).to(g["y"].device)
-    y_c = to_np_u16(g["y"].index_select(0, gather))
-    compact = np.where(sub >= 0, np.arange(sub.size).reshape(sub.shape), -1).astype(np.int32)
-    ref_out = orc.combine(y_c, case["w"][toks], compact, w.H)
-    got = to_np_u16(g["out"].index_select(0, torch.from_numpy(toks).to(g["out"].device)))
-    d = bf16_ulp_diff(got, ref_out)
-    assert d.max() <= 1, f"combine differs by {d.max()} bf16 ulp"
-    return float((d == 0).mean())
+    exact = 0
+    worst = 0
+    for c0 in range(0, toks.size, CHUNK_TOKENS):
+        part = toks[c0:c0 + CHUNK_TOKENS]
+        sub = dst[part]
+        flat = sub.ravel()
+        gather = torch.from_numpy(np.where(flat >= 0, flat, 0).astype(np.int64)).to(g["y"].device)
+        y_c = to_np_u16(g["y"].index_select(0, gather))
+        compact = np.where(sub >= 0, np.arange(sub.size).reshape(sub.shape), -1).astype(np.int32)
+        ref_out = orc.combine(y_c, case["w"][part], compact, w.H)
+        got = to_np_u16(g["out"].index_select(0, torch.from_numpy(part).to(g["out"].device)))
+        d = bf16_ulp_diff(got, ref_out)
+        worst = max(worst, int(d.max()))
+        exact += int((d == 0).sum())
+    assert worst <= 1, f"combine differs by {worst} bf16 ulp"
+    return exact / float(toks.size * w.H)
+
+
+def check_dispatch_mn(w, case, L, out_rows, out_scales, ref, orc=None, sentinel=None):
+    """MN-major UE8M0 dispatch: rows bit-exact on every valid row; scale words
+    bit-exact against the oracle's re-layout of its row-major words."""
+    orc = orc or oracle.default()
+    cap_rows = L.rows_capacity
+    o_rows, o_sc, _ = orc.dispatch(case["x"], ref["dst_row"], max(cap_rows, 1), "fp8_ue8m0")
+    valid = np.nonzero(ref["row_src"] >= 0)[0]
+    if valid.size == 0:
+        return
+    got_rows = out_rows[:ref["rows"]].cpu().numpy()
+    assert np.array_equal(got_rows[valid], o_rows[valid]), "dispatched rows differ"
+    mn = orc.scales_mn_major(o_sc[:cap_rows], w.layout, E=w.E, cap=w.cap)
+    got = out_scales.reshape(-1).cpu().numpy()
+    assert got.size == mn.size
+    P = o_sc.shape[1]
+    if w.layout == "masked":
+        stride = (w.cap + 3) // 4 * 4
+        pos = ((valid // w.cap)[:, None] * P + np.arange(P)[None, :]) * stride + \
+            (valid % w.cap)[:, None]
+    else:
+        stride = (cap_rows + 3) // 4 * 4
+        pos = np.arange(P)[None, :] * stride + valid[:, None]
+    assert np.array_equal(got[pos.ravel()], mn[pos.ravel()]), "MN-major scale words differ"

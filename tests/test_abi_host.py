@@ -114,6 +114,25 @@ def test_host_validation_returns_before_any_launch(lib):
     assert lib.ep_status_str(6).decode().startswith("EP_ERR_TIMEOUT")
 
 
+def test_noalloc_checks_arguments_before_its_scratch_size(lib):
+    """ep_layout_noalloc gives ep_layout's code for bad arguments even on a
+    shape too large for its fixed array, and EP_ERR_CAPACITY only for a
+    well-formed call; all before any CUDA call."""
+    INVALID, CAPACITY = 1, 2
+    from combine_expert_histogram_gb300 import binding
+    L = _layout(num_tokens=70000, num_experts=1024)
+    assert lib.ep_layout_workspace_bytes(ctypes.byref(L)) > binding.NOALLOC_SCRATCH_BYTES
+    assert lib.ep_layout_noalloc(ctypes.c_void_p(4096), ctypes.byref(L), None) == INVALID
+    L.dst_row = L.expert_count = L.expert_offset = L.status = 256
+    assert lib.ep_layout_noalloc(None, ctypes.byref(L), None) == INVALID
+    assert lib.ep_layout_noalloc(ctypes.c_void_p(4098), ctypes.byref(L), None) == INVALID
+    L.max_tokens = 8
+    assert lib.ep_layout_noalloc(ctypes.c_void_p(4096), ctypes.byref(L), None) == CAPACITY
+    L.max_tokens = 0
+    assert lib.ep_layout_noalloc(ctypes.c_void_p(4096), ctypes.byref(L), None) == CAPACITY
+    assert lib.ep_layout_noalloc(ctypes.c_void_p(4096), None, None) == INVALID
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     from combine_expert_histogram_gb300 import binding

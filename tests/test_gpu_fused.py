@@ -139,7 +139,8 @@ QUANTS = ["none", "fp8_f32", "fp8_ue8m0", "mxfp8", "fp8_ue8m0_mn"]
 def test_fused_fuzz_equals_two_calls(seed):
     """Random decode-sized shapes (up to 8192 entries, so one kernel) with -1
     ids, repeated experts and small masked capacities: every output array
-    equals ep_layout followed by ep_dispatch."""
+    equals ep_layout followed by ep_dispatch, and the one call's outputs equal
+    the oracle's."""
     rng = np.random.default_rng(500 + seed)
     K = int(rng.integers(1, 33))
     T = int(rng.integers(1, 8192 // K + 1))
@@ -182,6 +183,15 @@ def test_fused_fuzz_equals_two_calls(seed):
     if s1 is not None:
         assert torch.equal(s1.view(torch.int32), s2.view(torch.int32)), "scales differ"
     assert torch.equal(rw1.view(torch.int32), rw2.view(torch.int32)), "row weights differ"
+    # the one call against the oracle too: every layout array and status, every
+    # valid row, scale word and row weight, sentinels on the rows left empty
+    case = dict(idx=idx, w=wts, x=x)
+    res = dict(L=L, rows=L.rows_capacity, out_rows=r2, out_scales=s2, row_w=rw2)
+    ref = gh.check_layout(w, case, res)
+    if quant == "fp8_ue8m0_mn":
+        gh.check_dispatch_mn(w, case, L, r2, s2, ref)
+    else:
+        gh.check_dispatch(w, case, res, ref)
 
 
 @pytest.mark.parametrize("layout", ["contig", "masked"])
