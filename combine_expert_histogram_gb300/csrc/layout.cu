@@ -14,13 +14,14 @@
 //   * lanes holding the same expert in a round find each other with
 //     ceil(log2(E+1)) independent __ballot_sync's (one per bit of the id);
 //     the mask is kept per round and reused for ranking;
-//   * up to 1024 entries one 1024-thread CTA does everything in one kernel;
-//     above that, tiles of 1024 entries (2048 beyond 32768) on 256-thread
-//     CTAs, so that the ballot work of decode-sized batches spreads over SMs;
-//   * up to 4096 entries the tiles still run as one kernel: every tile CTA
-//     recounts all entries with shared-memory atomics (a few per thread) for
-//     the expert totals and its tile's base, so no CTA depends on another and
-//     CTA 0 alone writes the status word;
+//   * up to kClusterMaxEntries entries (decode-sized batches) one kernel of
+//     one thread-block cluster does everything (cluster_layout_kernel): each
+//     CTA ranks its own slice of the entries (__match_any_sync peer masks,
+//     per-warp counts), publishes its expert histogram in shared memory, and
+//     after a cluster barrier reads its peers' histograms through distributed
+//     shared memory for the expert totals and its slice's base; the cluster's
+//     CTAs share the row_src fill; no workspace, and no CTA reads more than
+//     its own slice of topk_idx;
 //   * beyond that, tile_hist_kernel counts each tile's experts (shared-memory
 //     atomics; counts need no order) into the scratch workspace [tiles][E],
 //     then assign_kernel (launched as a programmatic dependent, so its loads
@@ -346,12 +347,325 @@ __global__ void __launch_bounds__(NT) assign_kernel(AssignArgs a) {
     }
 }
 
+// ---- decode-sized batches: one thread-block cluster ----
+
+constexpr int kClThreads = 256;          // threads per CTA of the cluster kernel
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClTargetPerCta = 256;     // entries per CTA aimed for (one round per warp)
+constexpr int kClMaxCtas = 16;           // CTAs per cluster (16 needs the non-portable opt-in)
+constexpr int kClusterMaxEntries = 16384;  // 8 CTAs of 8 rounds per warp hold it too
+
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_nctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// All threads of every CTA of the cluster take part (uniform control flow).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Shared-memory word `p` of this CTA, as seen in the CTA of cluster rank `rank`.
+__device__ __forceinline__ int32_t ld_peer(const int32_t *p, unsigned rank) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    uint32_t ra;
+    int32_t v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+// v = -1 for rows [r0, r1) of row_src; 16-byte stores where the address allows.
+__device__ __forceinline__ void fill_minus_one(int32_t *row_src, int r0, int r1, int lane) {
+    if (r0 >= r1) return;
+    const int head = (int)((16 - (reinterpret_cast<uintptr_t>(row_src + r0) & 15)) & 15) / 4;
+    const int a = min(r1, r0 + head);        // first 16-byte-aligned row (or r1)
+    const int b = a + ((r1 - a) & ~3);       // end of the aligned run
+    if (lane < a - r0) row_src[r0 + lane] = -1;
+    const int4 m1 = make_int4(-1, -1, -1, -1);
+    for (int r = a + 4 * lane; r < b; r += 128) *reinterpret_cast<int4 *>(row_src + r) = m1;
+    if (lane < r1 - b) row_src[b + lane] = -1;
+}
+
+struct ClusterArgs {
+    const int32_t *idx;
+    int TK, E, R, masked, align, cap;
+    int chunk;  // entries per warp (32 * rounds)
+    int32_t *dst_row, *row_src, *count, *offset, *rank_rows, *status;
+};
+
+// Grid: one or more clusters.  Every cluster lays out all TK entries the
+// same way (CTA c of a cluster owns entries [c * 8 * chunk, (c + 1) * 8 *
+// chunk), warp w of it the chunk at w * chunk), so (CTA, warp, round, lane)
+// order is entry order and the slot of an entry is
+//   (entries of its expert in lower CTAs) + (in lower warps of its CTA)
+//   + (in earlier rounds of its warp) + (in lower lanes of its round).
+// Cluster 0 writes the layout arrays; the row_src fill of empty rows is
+// shared by the warps of all clusters (more clusters spread a large masked
+// fill over more SMs).
+template <int ROUNDS>
+__global__ void __launch_bounds__(kClThreads) cluster_layout_kernel(ClusterArgs a) {
+    extern __shared__ int32_t csm[];
+    const int E = a.E;
+    int32_t *wh = csm;                  // [kClWarps][E] per-warp counts, then warp bases
+    int32_t *hist = wh + kClWarps * E;  // [E+1] this CTA's expert counts; [E] = bad-id flag
+    int32_t *tot = hist + E + 1;        // [E] expert totals
+    int32_t *base = tot + E;            // [E] entries of each expert in lower CTAs
+    int32_t *off = base + E;            // [E+1] first row of each expert
+    __shared__ int32_t scan_tmp[kClWarps];
+
+    // The layout's only kernel: wait for the previous kernel on the stream (it
+    // may have produced topk_idx, and may still read these arrays) before
+    // anything else; then the next kernel (dispatch) may start.
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
+    const int cluster = (int)(blockIdx.x / csize);
+    const bool writer = cluster == 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int w0 = ((int)crank * kClWarps + warp) * a.chunk;
+    const int w1 = min(a.TK, w0 + a.chunk);
+
+    // 1. this warp's entries, all loads in flight at once; the warp zeroes
+    //    its own count row meanwhile
+    int ev[ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int i = w0 + r * 32 + lane;
+        ev[r] = i < w1 ? __ldg(a.idx + i) : -1;
+    }
+    int32_t *row = wh + warp * E;
+    for (int e = lane; e < E; e += 32) row[e] = 0;
+    __syncwarp();
+
+    // 2. per round: peers with the same expert; rank among them; warp counts
+    int rank[ROUNDS];
+    int bad = 0;
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int e0 = ev[r];
+        bad |= e0 < -1 || e0 >= E;
+        const int e = (e0 >= 0 && e0 < E) ? e0 : E;  // E = no expert
+        ev[r] = e;
+        const unsigned peers = __match_any_sync(kFullMask, e);
+        const int before = e < E ? row[e] : 0;
+        __syncwarp();
+        if (e < E && lane == __ffs(peers) - 1) row[e] = before + __popc(peers);
+        __syncwarp();
+        rank[r] = before + __popc(peers & lanemask_lt());
+    }
+    bad = __syncthreads_or(bad);
+
+    // 3. warp counts -> warp bases within the CTA; the CTA's histogram
+    for (int e = threadIdx.x; e < E; e += kClThreads) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < kClWarps; ++w) {
+            const int c = wh[w * E + e];
+            wh[w * E + e] = run;
+            run += c;
+        }
+        hist[e] = run;
+    }
+    if (threadIdx.x == 0) hist[E] = bad;
+
+    // 4. every CTA's histogram is visible to the cluster; totals and this
+    //    CTA's base from all of them (distributed shared memory)
+    cluster_arrive();
+    cluster_wait();
+    int any_bad = 0;
+    for (int e = threadIdx.x; e < E; e += kClThreads) {
+        int t = 0, b = 0;
+        for (unsigned c = 0; c < csize; ++c) {
+            const int v = ld_peer(hist + e, c);
+            t += v;
+            b += c < crank ? v : 0;
+        }
+        tot[e] = t;
+        base[e] = b;
+    }
+    if (writer && crank == 0 && threadIdx.x < csize) any_bad = ld_peer(hist + E, threadIdx.x);
+    // done reading the peers (nothing to publish: relaxed); they may exit
+    // once every thread of the cluster has arrived here
+    cluster_arrive_relaxed();
+    any_bad = __syncthreads_or(any_bad);
+
+    // 5. offsets: e*cap (masked) or the padded exclusive scan (contiguous)
+    const int align = a.align, cap = a.cap, masked = a.masked;
+    if (masked) {
+        for (int e = threadIdx.x; e <= E; e += kClThreads) off[e] = e * cap;
+        __syncthreads();
+    } else {
+        block_exclusive_scan<kClThreads>(
+            E, [&](int e) { return round_up_pow2(tot[e], align); }, off, scan_tmp);
+    }
+
+    if (writer) {
+        // 6. stable slots of this warp's entries
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+            const int i = w0 + r * 32 + lane;
+            if (i < w1) {
+                const int e = ev[r];
+                int dst = -1;
+                if (e < E) {
+                    const int slot = base[e] + row[e] + rank[r];
+                    if (!(masked && slot >= cap)) dst = off[e] + slot;
+                }
+                a.dst_row[i] = dst;
+                if (dst >= 0 && a.row_src) a.row_src[dst] = i;
+            }
+        }
+        // 7. CTA 0: counts, offsets, rank rows, status
+        if (crank == 0) {
+            int over = 0;
+            for (int e = threadIdx.x; e < E; e += kClThreads) {
+                a.count[e] = tot[e];
+                a.offset[e] = off[e];
+                over |= masked && tot[e] > cap;
+            }
+            over = __syncthreads_or(over);
+            if (threadIdx.x == 0) {
+                a.offset[E] = off[E];
+                *a.status = any_bad ? EP_ERR_BAD_EXPERT_ID : over ? EP_ERR_CAPACITY : EP_OK;
+            }
+            if (a.rank_rows) {  // one warp per rank: sum of its experts' counts
+                const int per = E / a.R;
+                for (int rr = warp; rr < a.R; rr += kClWarps) {
+                    int sum = 0;
+                    for (int e = rr * per + lane; e < (rr + 1) * per; e += 32) sum += tot[e];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFullMask, sum, o);
+                    if (lane == 0) a.rank_rows[rr] = sum;
+                }
+            }
+        }
+    }
+
+    // 8. row_src = -1 on padding rows (contiguous) and empty slots (masked),
+    //    one warp per expert across all clusters
+    if (a.row_src) {
+        const int gw = (int)blockIdx.x * kClWarps + warp, nw = (int)gridDim.x * kClWarps;
+        for (int e = gw; e < E; e += nw) {
+            const int r0 = off[e] + (masked ? min(tot[e], cap) : tot[e]);
+            const int r1 = masked ? off[e] + cap : off[e + 1];
+            fill_minus_one(a.row_src, r0, r1, lane);
+        }
+    }
+    // no CTA leaves while a peer may still read its histogram
+    cluster_wait();
+}
+
+using ClusterKernel = void (*)(ClusterArgs);
+
+ClusterKernel cluster_kernel(int rounds) {
+    switch (rounds) {
+        case 1: return cluster_layout_kernel<1>;
+        case 2: return cluster_layout_kernel<2>;
+        case 4: return cluster_layout_kernel<4>;
+        default: return cluster_layout_kernel<8>;
+    }
+}
+
+}  // namespace
+
+namespace {
+
+// CTAs of the cluster kernel for TK entries with at most max_ctas per
+// cluster, and the entries per warp (32 x a power-of-two number of rounds).
+void cluster_shape(long long TK, int max_ctas, int *ctas, int *chunk) {
+    long long c = (TK + kClTargetPerCta - 1) / kClTargetPerCta;
+    if (c < 1) c = 1;
+    if (c > max_ctas) c = max_ctas;
+    int rounds = 1;
+    while ((long long)rounds * 32 * kClWarps * c < TK) rounds *= 2;
+    // as few CTAs as the rounds allow (fewer peers to read)
+    while (c > 1 && (long long)rounds * 32 * kClWarps * (c - 1) >= TK) --c;
+    *ctas = (int)c;
+    *chunk = 32 * rounds;
+}
+
+// Clusters of the cluster kernel: one, plus more to share a large masked
+// row_src fill (about 8192 rows per CTA).
+int fill_clusters(const ep_layout_t &L, int ctas) {
+    if (L.kind != EP_LAYOUT_MASKED || L.row_src == nullptr) return 1;
+    const long long rows = (long long)L.num_experts * L.capacity;
+    const long long per = (long long)ctas * 8192;
+    long long n = (rows + per - 1) / per;
+    if (n < 1) n = 1;
+    if (n > 4) n = 4;
+    return (int)n;
+}
+
+// 16 CTAs per cluster where the device can co-schedule them (with the
+// largest shared memory the kernel asks for), else the portable 8; once per
+// device.
+int max_cluster_ctas() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+    if (cached[dev] == 0) {
+        int best = 8;
+        const size_t smem = sizeof(int32_t) * (12 * (size_t)EP_MAX_EXPERTS + 2);
+        const ClusterKernel k = cluster_kernel(8);
+        if (allow_dynamic_smem(k, smem) == cudaSuccess &&
+            cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(kClMaxCtas);
+            cfg.blockDim = dim3(kClThreads);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = kClMaxCtas;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess &&
+                n >= 1)
+                best = kClMaxCtas;
+        }
+        cudaGetLastError();  // a refused query leaves no error behind
+        cached[dev] = best;
+    }
+    return cached[dev];
+}
+
 }  // namespace
 
 LayoutPlan layout_plan(const ep_layout_t &L) {
     LayoutPlan p{};
     const long long TK = (long long)L.num_tokens * L.num_topk;
     int warps;
+    if (TK <= kClusterMaxEntries) {
+        // one cluster (its CTA count is chosen at launch: 8 or 16 at most)
+        int ctas, chunk;
+        cluster_shape(TK, kClMaxCtas, &ctas, &chunk);
+        p.cluster = true;
+        p.threads = kClThreads;
+        p.tiles = ctas;
+        p.grid = ctas;
+        p.passes = 1;
+        p.chunk = chunk;
+        p.tile = chunk * kClWarps;
+        p.self_hist = false;
+        p.smem = sizeof(int32_t) * (12 * (size_t)L.num_experts + 2);
+        p.ws_bytes = 0;
+        return p;
+    }
     if (TK <= kSmallMax) {
         // one 1024-thread CTA, one 32-entry round per warp
         p.threads = kSmallThreads;
@@ -395,6 +709,48 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     const LayoutPlan p = layout_plan(L);
     const int TK = L.num_tokens * L.num_topk;
     const int E = L.num_experts;
+    if (p.cluster) {
+        ClusterArgs c;
+        c.idx = topk_idx;
+        c.TK = TK;
+        c.E = E;
+        c.R = L.num_ranks;
+        c.masked = L.kind == EP_LAYOUT_MASKED;
+        c.align = c.masked ? 1 : L.align;
+        c.cap = c.masked ? L.capacity : 0;
+        int ctas;
+        cluster_shape(TK, max_cluster_ctas(), &ctas, &c.chunk);
+        const int nclusters = fill_clusters(L, ctas);
+        c.dst_row = L.dst_row;
+        c.row_src = L.row_src;
+        c.count = L.expert_count;
+        c.offset = L.expert_offset;
+        c.rank_rows = L.rank_rows;
+        c.status = L.status;
+        const ClusterKernel k = cluster_kernel(c.chunk / 32);
+        cudaError_t err = allow_dynamic_smem(k, p.smem);
+        if (err != cudaSuccess) return err;
+        if (ctas > 8) {
+            err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (err != cudaSuccess) return err;
+        }
+        // the layout's only kernel: programmatic, waiting for the previous kernel first
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(ctas * nclusters);
+        cfg.blockDim = dim3(kClThreads);
+        cfg.dynamicSmemBytes = p.smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = ctas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, k, c);
+    }
     AssignArgs a;
     a.idx = topk_idx;
     a.TK = TK;

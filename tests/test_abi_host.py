@@ -64,13 +64,14 @@ def test_sizing_helpers(lib):
     # hidden sizes up to EP_MAX_HIDDEN = 32768 (rows are staged in shared memory)
     assert lib.ep_scale_cols(32768, 1) == 256
     assert lib.ep_scale_cols(32768 + 128, 1) == -1
-    # up to 4096 entries one kernel and no scratch (one CTA up to 1024 entries, then
-    # tiles that each recount every entry); beyond, tiles of 1024 entries (2048 above
-    # 32768 entries) need tiles x E int32
+    # up to 16384 entries one kernel of one thread-block cluster and no scratch;
+    # beyond, tiles of 1024 entries (2048 above 32768 entries) need tiles x E int32
+    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=0))) == 0
     assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=128))) == 0
-    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=512))) == 0
-    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=513))) == 5 * 256 * 4
-    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=1025))) == 9 * 256 * 4
+    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=1024))) == 0
+    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=2048))) == 0
+    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=2049))) == 17 * 256 * 4
+    assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=4096))) == 32 * 256 * 4
     assert lib.ep_layout_workspace_bytes(ctypes.byref(_layout(num_tokens=16384))) == 64 * 256 * 4
 
 
