@@ -435,14 +435,16 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
 }
 
 // Slot j of token row xr into registers: 16 bf16 (two 16-byte loads) for the
-// FP8 modes, 8 bf16 for bf16.
+// FP8 modes, 8 bf16 for bf16.  Coherent loads: the next token's slot is loaded
+// ahead of the current token's stores and must stay there (a non-coherent
+// load could be moved below them).
 template <int Q>
 __device__ __forceinline__ void load_slot(const uint16_t *xr, int j, uint4 &a, uint4 &b) {
     if (Q == EP_QUANT_NONE) {
-        a = ld_stream(xr + j * 8);
+        a = ld_stream_coh(xr + j * 8);
     } else {
-        a = ld_stream(xr + j * 16);
-        b = ld_stream(xr + j * 16 + 8);
+        a = ld_stream_coh(xr + j * 16);
+        b = ld_stream_coh(xr + j * 16 + 8);
     }
 }
 

@@ -32,6 +32,19 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
     return v;
 }
 
+// Streaming 16-byte load (no L1 allocation) on the coherent path, for data
+// read once that must stay in flight across later stores: the assembler may
+// move a non-coherent load below a store (it knows the data is read-only),
+// which would serialise a "load the next row, store this one" loop; a coherent
+// load may alias the store and keeps its place.
+__device__ __forceinline__ uint4 ld_stream_coh(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 // Loads of what a programmatic predecessor wrote, issued after
 // griddepcontrol.wait.  A const __restrict__ pointer or __ldg lets the
 // compiler treat the data as read-only for the whole kernel (non-coherent

@@ -19,9 +19,9 @@
 //     CTA ranks its own slice of the entries (__match_any_sync peer masks,
 //     per-warp counts), publishes its expert histogram in shared memory, and
 //     after a cluster barrier reads its peers' histograms through distributed
-//     shared memory for the expert totals and its slice's base; the cluster's
-//     CTAs share the row_src fill; no workspace, and no CTA reads more than
-//     its own slice of topk_idx;
+//     shared memory (four peers' loads in flight at once) for the expert
+//     totals and its slice's base; the CTAs share the row_src fill; no
+//     workspace, and no CTA reads more than its own slice of topk_idx;
 //   * beyond that, tile_hist_kernel counts each tile's experts (shared-memory
 //     atomics; counts need no order) into the scratch workspace [tiles][E],
 //     then assign_kernel (launched as a programmatic dependent, so its loads
@@ -375,14 +375,29 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Shared-memory word `p` of this CTA, as seen in the CTA of cluster rank `rank`.
-__device__ __forceinline__ int32_t ld_peer(const int32_t *p, unsigned rank) {
+// The shared-memory word that `p` names, read from the CTAs of cluster ranks
+// c0 .. c0+3 (distributed shared memory), all four loads in flight at once.
+// Ranks at or past csize read rank 0 and give 0.
+__device__ __forceinline__ void ld_peers4(const int32_t *p, unsigned c0, unsigned csize,
+                                          int32_t v[4]) {
     const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
-    uint32_t ra;
-    int32_t v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
-    return v;
+    const unsigned r0 = c0 < csize ? c0 : 0, r1 = c0 + 1 < csize ? c0 + 1 : 0;
+    const unsigned r2 = c0 + 2 < csize ? c0 + 2 : 0, r3 = c0 + 3 < csize ? c0 + 3 : 0;
+    asm volatile(
+        "{\n\t.reg .b32 a0, a1, a2, a3;\n\t"
+        "mapa.shared::cluster.u32 a0, %4, %5;\n\t"
+        "mapa.shared::cluster.u32 a1, %4, %6;\n\t"
+        "mapa.shared::cluster.u32 a2, %4, %7;\n\t"
+        "mapa.shared::cluster.u32 a3, %4, %8;\n\t"
+        "ld.shared::cluster.s32 %0, [a0];\n\t"
+        "ld.shared::cluster.s32 %1, [a1];\n\t"
+        "ld.shared::cluster.s32 %2, [a2];\n\t"
+        "ld.shared::cluster.s32 %3, [a3];\n\t}"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+        : "r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+        : "memory");
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = c0 + j < csize ? v[j] : 0;
 }
 
 // v = -1 for rows [r0, r1) of row_src; 16-byte stores where the address allows.
@@ -411,8 +426,8 @@ struct ClusterArgs {
 //   (entries of its expert in lower CTAs) + (in lower warps of its CTA)
 //   + (in earlier rounds of its warp) + (in lower lanes of its round).
 // Cluster 0 writes the layout arrays; the row_src fill of empty rows is
-// shared by the warps of all clusters (more clusters spread a large masked
-// fill over more SMs).
+// shared by the warps of all clusters (a second cluster spreads a large
+// masked fill over more SMs).
 template <int ROUNDS>
 __global__ void __launch_bounds__(kClThreads) cluster_layout_kernel(ClusterArgs a) {
     extern __shared__ int32_t csm[];
@@ -423,6 +438,7 @@ __global__ void __launch_bounds__(kClThreads) cluster_layout_kernel(ClusterArgs 
     int32_t *base = tot + E;            // [E] entries of each expert in lower CTAs
     int32_t *off = base + E;            // [E+1] first row of each expert
     __shared__ int32_t scan_tmp[kClWarps];
+    __shared__ int32_t s_flags;         // bit 0: a bad id; bit 1: a masked expert over capacity
 
     // The layout's only kernel: wait for the previous kernel on the stream (it
     // may have produced topk_idx, and may still read these arrays) before
@@ -431,8 +447,7 @@ __global__ void __launch_bounds__(kClThreads) cluster_layout_kernel(ClusterArgs 
     pdl_launch_dependents();
 
     const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
-    const int cluster = (int)(blockIdx.x / csize);
-    const bool writer = cluster == 0;
+    const bool writer = blockIdx.x < csize;  // cluster 0
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int w0 = ((int)crank * kClWarps + warp) * a.chunk;
     const int w1 = min(a.TK, w0 + a.chunk);
@@ -447,6 +462,7 @@ __global__ void __launch_bounds__(kClThreads) cluster_layout_kernel(ClusterArgs 
     }
     int32_t *row = wh + warp * E;
     for (int e = lane; e < E; e += 32) row[e] = 0;
+    if (threadIdx.x == 0) s_flags = 0;
     __syncwarp();
 
     // 2. per round: peers with the same expert; rank among them; warp counts
@@ -481,32 +497,43 @@ __global__ void __launch_bounds__(kClThreads) cluster_layout_kernel(ClusterArgs 
     if (threadIdx.x == 0) hist[E] = bad;
 
     // 4. every CTA's histogram is visible to the cluster; totals and this
-    //    CTA's base from all of them (distributed shared memory)
+    //    CTA's base from all of them, plus the error flags
     cluster_arrive();
     cluster_wait();
-    int any_bad = 0;
+    const int cap = a.cap, masked = a.masked;
+    int flags = 0;
     for (int e = threadIdx.x; e < E; e += kClThreads) {
         int t = 0, b = 0;
-        for (unsigned c = 0; c < csize; ++c) {
-            const int v = ld_peer(hist + e, c);
-            t += v;
-            b += c < crank ? v : 0;
+        for (unsigned c = 0; c < csize; c += 4) {
+            int v[4];
+            ld_peers4(hist + e, c, csize, v);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                t += v[j];
+                b += c + j < crank ? v[j] : 0;
+            }
         }
         tot[e] = t;
         base[e] = b;
+        if (masked && t > cap) flags |= 2;
     }
-    if (writer && crank == 0 && threadIdx.x < csize) any_bad = ld_peer(hist + E, threadIdx.x);
+    if (threadIdx.x < csize) {
+        int v[4];
+        ld_peers4(hist + E, threadIdx.x, threadIdx.x + 1, v);  // peer threadIdx.x's flag
+        if (v[0]) flags |= 1;
+    }
     // done reading the peers (nothing to publish: relaxed); they may exit
     // once every thread of the cluster has arrived here
     cluster_arrive_relaxed();
-    any_bad = __syncthreads_or(any_bad);
+    if (flags) atomicOr(&s_flags, flags);
 
     // 5. offsets: e*cap (masked) or the padded exclusive scan (contiguous)
-    const int align = a.align, cap = a.cap, masked = a.masked;
+    const int align = a.align;
     if (masked) {
         for (int e = threadIdx.x; e <= E; e += kClThreads) off[e] = e * cap;
         __syncthreads();
     } else {
+        __syncthreads();
         block_exclusive_scan<kClThreads>(
             E, [&](int e) { return round_up_pow2(tot[e], align); }, off, scan_tmp);
     }
@@ -527,19 +554,18 @@ __global__ void __launch_bounds__(kClThreads) cluster_layout_kernel(ClusterArgs 
                 if (dst >= 0 && a.row_src) a.row_src[dst] = i;
             }
         }
-        // 7. CTA 0: counts, offsets, rank rows, status
-        if (crank == 0) {
-            int over = 0;
-            for (int e = threadIdx.x; e < E; e += kClThreads) {
-                a.count[e] = tot[e];
-                a.offset[e] = off[e];
-                over |= masked && tot[e] > cap;
-            }
-            over = __syncthreads_or(over);
-            if (threadIdx.x == 0) {
-                a.offset[E] = off[E];
-                *a.status = any_bad ? EP_ERR_BAD_EXPERT_ID : over ? EP_ERR_CAPACITY : EP_OK;
-            }
+        // 7. counts and offsets, a slice of the experts per CTA; the status
+        //    word from CTA 0, the rank rows from the last CTA
+        for (int e = (int)crank * kClThreads + threadIdx.x; e < E; e += (int)csize * kClThreads) {
+            a.count[e] = tot[e];
+            a.offset[e] = off[e];
+        }
+        if (crank == 0 && threadIdx.x == 0) {
+            const int f = s_flags;
+            *a.status = (f & 1) ? EP_ERR_BAD_EXPERT_ID : (f & 2) ? EP_ERR_CAPACITY : EP_OK;
+        }
+        if (crank == csize - 1) {
+            if (threadIdx.x == 0) a.offset[E] = off[E];
             if (a.rank_rows) {  // one warp per rank: sum of its experts' counts
                 const int per = E / a.R;
                 for (int rr = warp; rr < a.R; rr += kClWarps) {
@@ -582,6 +608,12 @@ ClusterKernel cluster_kernel(int rounds) {
 
 namespace {
 
+// Dynamic shared memory of the cluster kernel: per-warp counts, the CTA's
+// histogram (+ bad-id flag), totals, bases and offsets.
+size_t cluster_smem(int E) {
+    return sizeof(int32_t) * ((size_t)kClWarps * E + 4 * (size_t)E + 2);
+}
+
 // CTAs of the cluster kernel for TK entries with at most max_ctas per
 // cluster, and the entries per warp (32 x a power-of-two number of rounds).
 void cluster_shape(long long TK, int max_ctas, int *ctas, int *chunk) {
@@ -596,16 +628,14 @@ void cluster_shape(long long TK, int max_ctas, int *ctas, int *chunk) {
     *chunk = 32 * rounds;
 }
 
-// Clusters of the cluster kernel: one, plus more to share a large masked
-// row_src fill (about 8192 rows per CTA).
+// Clusters of the cluster kernel: one, or two to share a large masked
+// row_src fill (the fill is bound by each SM's store rate, about 30 bytes
+// per clock; more than two clusters measured slower at the DeepSeek-V3
+// decode shape).
 int fill_clusters(const ep_layout_t &L, int ctas) {
     if (L.kind != EP_LAYOUT_MASKED || L.row_src == nullptr) return 1;
     const long long rows = (long long)L.num_experts * L.capacity;
-    const long long per = (long long)ctas * 8192;
-    long long n = (rows + per - 1) / per;
-    if (n < 1) n = 1;
-    if (n > 4) n = 4;
-    return (int)n;
+    return rows > (long long)ctas * 2048 ? 2 : 1;
 }
 
 // 16 CTAs per cluster where the device can co-schedule them (with the
@@ -617,7 +647,7 @@ int max_cluster_ctas() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
     if (cached[dev] == 0) {
         int best = 8;
-        const size_t smem = sizeof(int32_t) * (12 * (size_t)EP_MAX_EXPERTS + 2);
+        const size_t smem = cluster_smem(EP_MAX_EXPERTS);
         const ClusterKernel k = cluster_kernel(8);
         if (allow_dynamic_smem(k, smem) == cudaSuccess &&
             cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
@@ -662,7 +692,7 @@ LayoutPlan layout_plan(const ep_layout_t &L) {
         p.chunk = chunk;
         p.tile = chunk * kClWarps;
         p.self_hist = false;
-        p.smem = sizeof(int32_t) * (12 * (size_t)L.num_experts + 2);
+        p.smem = cluster_smem(L.num_experts);
         p.ws_bytes = 0;
         return p;
     }
@@ -728,7 +758,8 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
         c.rank_rows = L.rank_rows;
         c.status = L.status;
         const ClusterKernel k = cluster_kernel(c.chunk / 32);
-        cudaError_t err = allow_dynamic_smem(k, p.smem);
+        const size_t smem = cluster_smem(E);
+        cudaError_t err = allow_dynamic_smem(k, smem);
         if (err != cudaSuccess) return err;
         if (ctas > 8) {
             err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -738,7 +769,7 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(ctas * nclusters);
         cfg.blockDim = dim3(kClThreads);
-        cfg.dynamicSmemBytes = p.smem;
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;

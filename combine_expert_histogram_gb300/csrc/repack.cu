@@ -6,14 +6,18 @@
 // Byte copy, HBM-bound.  Every CTA scans m_e = min(count[e], cap) into shared
 // memory, then its warps walk the flat list of valid rows grid-stride; a
 // binary search over the prefix finds (expert, slot) of a flat row.  One warp
-// copies one row with 16-byte vectors (four loads in flight per lane) and its
-// scale words with 4-byte words.
+// copies one row: up to 8 KB of it (16 16-byte vectors per lane) and its scale
+// words are loaded before any of them is stored, so a row of the DeepSeek-V3
+// shape (7168 E4M3 bytes + 56 scale bytes) takes one memory round trip.  The
+// loads take the coherent path: non-coherent ones could be moved below the
+// stores by the assembler, one vector in flight per lane at a time.
 #include "ep_common.cuh"
 
 namespace ep {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
+constexpr int kVec = 16;  // 16-byte vectors per lane in flight (8 KB per warp)
 
 __global__ void __launch_bounds__(kThreads)
     repack_kernel(const uint8_t *__restrict__ rows, const uint8_t *__restrict__ row_scales,
@@ -40,6 +44,9 @@ __global__ void __launch_bounds__(kThreads)
     const int lane = threadIdx.x & 31;
     const int total = pre[E];
     const int warps = gridDim.x * (kThreads / 32);
+    const int words = scale_bytes / 4;
+    const uint32_t *ss_all = reinterpret_cast<const uint32_t *>(row_scales);
+    uint32_t *ds_all = reinterpret_cast<uint32_t *>(slab_scales);
     for (int r = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < total; r += warps) {
         int lo = 0, hi = E;  // pre[lo] <= r < pre[hi]
         while (hi - lo > 1) {
@@ -51,30 +58,37 @@ __global__ void __launch_bounds__(kThreads)
         const size_t dst = (size_t)lo * cap + s;
         const uint8_t *sp = rows + src * row_bytes;
         uint8_t *dp = slab + dst * row_bytes;
-        // four 16-byte loads in flight per lane before their stores
-        for (int b0 = lane * 16; b0 < row_bytes; b0 += 4 * 32 * 16) {
-            uint4 v[4];
+        // the first scale word of each lane travels with the first part of the row
+        uint32_t sw = 0;
+        if (lane < words)
+            sw = (uint32_t)ld_dep(reinterpret_cast<const int32_t *>(
+                mn_src_stride ? ss_all + (size_t)lane * mn_src_stride + src
+                              : ss_all + src * words + lane));
+        for (int b0 = 0; b0 < row_bytes; b0 += kVec * 32 * 16) {
+            uint4 v[kVec];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int b = b0 + u * 32 * 16;
-                v[u] = b < row_bytes ? ld_stream(sp + b) : make_uint4(0, 0, 0, 0);
+            for (int u = 0; u < kVec; ++u) {
+                const int b = b0 + (u * 32 + lane) * 16;
+                v[u] = b < row_bytes ? ld_stream_coh(sp + b) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int b = b0 + u * 32 * 16;
+            for (int u = 0; u < kVec; ++u) {
+                const int b = b0 + (u * 32 + lane) * 16;
                 if (b < row_bytes) st_v4(dp + b, v[u]);
             }
         }
-        if (scale_bytes && mn_src_stride) {
-            const uint32_t *ss = reinterpret_cast<const uint32_t *>(row_scales);
-            uint32_t *ds = reinterpret_cast<uint32_t *>(slab_scales);
-            const int words = scale_bytes / 4;
-            for (int b = lane; b < words; b += 32)
-                ds[((size_t)lo * words + b) * mn_dst_stride + s] = __ldg(ss + (size_t)b * mn_src_stride + src);
-        } else if (scale_bytes) {
-            const uint32_t *ss = reinterpret_cast<const uint32_t *>(row_scales + src * scale_bytes);
-            uint32_t *ds = reinterpret_cast<uint32_t *>(slab_scales + dst * scale_bytes);
-            for (int b = lane; b < scale_bytes / 4; b += 32) ds[b] = __ldg(ss + b);
+        if (lane < words) {
+            if (mn_src_stride)
+                ds_all[((size_t)lo * words + lane) * mn_dst_stride + s] = sw;
+            else
+                ds_all[dst * words + lane] = sw;
+        }
+        for (int b = lane + 32; b < words; b += 32) {  // rows of more than 32 scale words
+            if (mn_src_stride)
+                ds_all[((size_t)lo * words + b) * mn_dst_stride + s] =
+                    __ldg(ss_all + (size_t)b * mn_src_stride + src);
+            else
+                ds_all[dst * words + b] = __ldg(ss_all + src * words + b);
         }
     }
 }
@@ -98,10 +112,11 @@ cudaError_t launch_masked_repack(const ep_layout_t &L, const void *rows,
         mn_src = (int)((rows_cap + 3) / 4 * 4);
         mn_dst = (cap + 3) / 4 * 4;
     }
-    // Enough warps to keep HBM busy: the valid rows number at most T*K.
+    // Enough warps to keep HBM busy (with a row of up to 8 KB in flight per
+    // warp, 16 warps per SM hold ~18 MB); the valid rows number at most T*K.
     const long long rows_max = (long long)L.num_tokens * L.num_topk;
     long long blocks = (rows_max + kThreads / 32 - 1) / (kThreads / 32);
-    const long long limit = 4LL * sm_count();
+    const long long limit = 2LL * sm_count();
     if (blocks > limit) blocks = limit;
     if (blocks < 1) blocks = 1;
     const size_t smem = sizeof(int32_t) * (size_t)(E + 1);
