@@ -804,6 +804,72 @@ def measure_rank_dedup(ep, dev, reps=10):
             "direct_dispatch_us": round(t_direct, 2)}
 
 
+def numa_placement(t) -> dict:
+    """NUMA nodes of the host, and the nodes holding the pages of pinned tensor t
+    (from /proc/self/numa_maps; Linux only)."""
+    import glob
+    nodes = {}
+    for n in sorted(glob.glob("/sys/devices/system/node/node[0-9]*")):
+        try:
+            nodes[os.path.basename(n)] = open(n + "/cpulist").read().strip()
+        except OSError:
+            pass
+    lo, hi = t.data_ptr(), t.data_ptr() + t.numel() * t.element_size()
+    pages = {}
+    try:
+        for line in open("/proc/self/numa_maps"):
+            f = line.split()
+            if lo <= int(f[0], 16) < hi:
+                for tok in f:
+                    if tok[:1] == "N" and "=" in tok:
+                        k, v = tok.split("=")
+                        pages[k] = pages.get(k, 0) + int(v)
+    except (OSError, ValueError):
+        pass
+    return {"host_nodes_cpus": nodes, "pinned_pages_by_node": pages}
+
+
+def link_rates(h, d, stream) -> dict:
+    """Host->device, device->host and both at once (two streams), GB/s, on
+    the pinned host tensor h and a device tensor d of the same bytes."""
+    import torch
+    other = torch.cuda.Stream(device=d.device)
+    hb = torch.empty_like(h, pin_memory=True)
+    db = torch.empty_like(d)
+    nbytes = h.numel() * h.element_size()
+
+    def timed(fn):
+        best = None
+        for _ in range(3):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        return best
+
+    def up():
+        with torch.cuda.stream(stream):
+            d.copy_(h, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(stream):
+            hb.copy_(db, non_blocking=True)
+
+    def both():
+        up()
+        with torch.cuda.stream(other):
+            hb.copy_(db, non_blocking=True)
+
+    tb = timed(both)
+    return {"h2d_GBps": round(nbytes / timed(up) / 1e9, 1),
+            "d2h_GBps": round(nbytes / timed(down) / 1e9, 1),
+            "both_at_once_GBps_each": round(nbytes / tb / 1e9, 1),
+            "bytes": nbytes, "method": "one cudaMemcpyAsync per direction from pinned memory, "
+                                        "best of 3; both: two streams"}
+
+
 def measure_e2e(ep, w, L, idx, wts, x, y_dev, out_rows, out_scales, dev, stream, args):
     """Same metric through the public API with inputs in pinned host memory:
     every step copies x, topk_idx, topk_w and the expert outputs y host->device,
@@ -876,9 +942,12 @@ def measure_e2e(ep, w, L, idx, wts, x, y_dev, out_rows, out_scales, dev, stream,
     t1.record(down)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / n
+    link = link_rates(h_x, bufs[0]["x"], up)
+    link.update(numa_placement(h_x))
     return {"value": w.T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": n,
-            "pipelined": "double-buffered inputs; copies up, compute, copies down overlap across steps"}
+            "pipelined": "double-buffered inputs; copies up, compute, copies down overlap across steps",
+            "host_link": link}
 
 
 def main():
