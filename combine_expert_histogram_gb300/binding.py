@@ -305,8 +305,8 @@ def ep_layout_dispatch(topk_idx: torch.Tensor, layout: Layout, x: torch.Tensor,
                        out_scales: Optional[torch.Tensor] = None,
                        topk_w: Optional[torch.Tensor] = None, row_w: Optional[torch.Tensor] = None,
                        stream=None):
-    """ep_layout into ``layout`` and ep_dispatch of x, in one call (one kernel for
-    decode-sized batches).  Returns (out_rows, out_scales, row_w) like ep_dispatch."""
+    """ep_layout into ``layout`` and ep_dispatch of x, in one call (the two
+    kernels back to back).  Returns (out_rows, out_scales, row_w) like ep_dispatch."""
     if topk_idx.dtype != torch.int32 or topk_idx.dim() != 2:
         raise ValueError("topk_idx must be int32 [T, K]")
     if x.dtype != torch.bfloat16:

@@ -1,0 +1,346 @@
+// The decode-sized layout (up to kClusterMaxEntries top-k entries) computed
+// by one thread-block cluster: the device body of the layout kernel in
+// csrc/layout.cu, and its host-side sizing and launch.
+//
+// The layout step that DeepEP V2's dispatch performs internally ("infers the
+// layout from topk_idx", SGLang PR "moe: add DeepEP V2 ElasticBuffer support
+// to MoE token dispatcher", section "Motivation"), for the contiguous
+// (prefill) and masked (decode) layouts of SGLang PR "[Feature] Add DeepEPv2
+// (ElasticBuffer) MoE A2A backend", section "Supported scope".
+#pragma once
+
+#include "ep_common.cuh"
+
+namespace ep {
+namespace cl {
+
+constexpr int kClThreads = 256;          // threads per CTA of the cluster kernel
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClTargetPerCta = 256;     // entries per CTA aimed for (one round per warp)
+constexpr int kClMaxCtas = 16;           // CTAs per cluster (16 needs the non-portable opt-in)
+constexpr int kClusterMaxEntries = 16384;  // 8 CTAs of 8 rounds per warp hold it too
+
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_nctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// All threads of every CTA of the cluster take part (uniform control flow).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared-memory word that `p` names, read from the CTAs of cluster ranks
+// c0 .. c0+3 (distributed shared memory), all four loads in flight at once.
+// Ranks at or past csize read rank 0 and give 0.
+__device__ __forceinline__ void ld_peers4(const int32_t *p, unsigned c0, unsigned csize,
+                                          int32_t v[4]) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    const unsigned r0 = c0 < csize ? c0 : 0, r1 = c0 + 1 < csize ? c0 + 1 : 0;
+    const unsigned r2 = c0 + 2 < csize ? c0 + 2 : 0, r3 = c0 + 3 < csize ? c0 + 3 : 0;
+    asm volatile(
+        "{\n\t.reg .b32 a0, a1, a2, a3;\n\t"
+        "mapa.shared::cluster.u32 a0, %4, %5;\n\t"
+        "mapa.shared::cluster.u32 a1, %4, %6;\n\t"
+        "mapa.shared::cluster.u32 a2, %4, %7;\n\t"
+        "mapa.shared::cluster.u32 a3, %4, %8;\n\t"
+        "ld.shared::cluster.s32 %0, [a0];\n\t"
+        "ld.shared::cluster.s32 %1, [a1];\n\t"
+        "ld.shared::cluster.s32 %2, [a2];\n\t"
+        "ld.shared::cluster.s32 %3, [a3];\n\t}"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+        : "r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+        : "memory");
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = c0 + j < csize ? v[j] : 0;
+}
+
+// v = -1 for rows [r0, r1) of row_src; 16-byte stores where the address allows.
+__device__ __forceinline__ void fill_minus_one(int32_t *row_src, int r0, int r1, int lane) {
+    if (r0 >= r1) return;
+    const int head = (int)((16 - (reinterpret_cast<uintptr_t>(row_src + r0) & 15)) & 15) / 4;
+    const int a = min(r1, r0 + head);        // first 16-byte-aligned row (or r1)
+    const int b = a + ((r1 - a) & ~3);       // end of the aligned run
+    if (lane < a - r0) row_src[r0 + lane] = -1;
+    const int4 m1 = make_int4(-1, -1, -1, -1);
+    for (int r = a + 4 * lane; r < b; r += 128) *reinterpret_cast<int4 *>(row_src + r) = m1;
+    if (lane < r1 - b) row_src[b + lane] = -1;
+}
+
+struct ClusterArgs {
+    const int32_t *idx;
+    int TK, E, R, masked, align, cap;
+    int chunk;  // entries per warp (32 * rounds)
+    int32_t *dst_row, *row_src, *count, *offset, *rank_rows, *status;
+};
+
+__host__ __device__ inline int round_up_pow2(int v, int a) { return (v + a - 1) & ~(a - 1); }
+
+// Grid: one or more clusters.  Every cluster lays out all TK entries the
+// same way (CTA c of a cluster owns entries [c * 8 * chunk, (c + 1) * 8 *
+// chunk), warp w of it the chunk at w * chunk), so (CTA, warp, round, lane)
+// order is entry order and the slot of an entry is
+//   (entries of its expert in lower CTAs) + (in lower warps of its CTA)
+//   + (in earlier rounds of its warp) + (in lower lanes of its round).
+// Cluster 0 writes the layout arrays; the row_src fill of empty rows is
+// shared by the warps of all clusters (a second cluster spreads a large
+// masked fill over more SMs).
+//
+// The body of a layout kernel of kClThreads threads per CTA: `csm` is
+// cluster_smem(E) bytes of the CTA's dynamic shared memory.  The caller has
+// waited for the previous kernel on the stream (griddepcontrol.wait) before
+// calling it; every thread of every CTA of the grid calls it.  Ends with a
+// cluster barrier.
+template <int ROUNDS>
+__device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_t *csm) {
+    const int E = a.E;
+    int32_t *wh = csm;                  // [kClWarps][E] per-warp counts, then warp bases
+    int32_t *hist = wh + kClWarps * E;  // [E+1] this CTA's expert counts; [E] = bad-id flag
+    int32_t *tot = hist + E + 1;        // [E] expert totals
+    int32_t *base = tot + E;            // [E] entries of each expert in lower CTAs
+    int32_t *off = base + E;            // [E+1] first row of each expert
+    __shared__ int32_t scan_tmp[kClWarps];
+    __shared__ int32_t s_flags;         // bit 0: a bad id; bit 1: a masked expert over capacity
+
+    const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
+    const bool writer = blockIdx.x < csize;  // cluster 0
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int w0 = ((int)crank * kClWarps + warp) * a.chunk;
+    const int w1 = min(a.TK, w0 + a.chunk);
+
+    // 1. this warp's entries, all loads in flight at once; the warp zeroes
+    //    its own count row meanwhile
+    int ev[ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int i = w0 + r * 32 + lane;
+        ev[r] = i < w1 ? __ldg(a.idx + i) : -1;
+    }
+    int32_t *row = wh + warp * E;
+    for (int e = lane; e < E; e += 32) row[e] = 0;
+    if (threadIdx.x == 0) s_flags = 0;
+    __syncwarp();
+
+    // 2. per round: peers with the same expert; rank among them; warp counts
+    int rank[ROUNDS];
+    int bad = 0;
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int e0 = ev[r];
+        bad |= e0 < -1 || e0 >= E;
+        const int e = (e0 >= 0 && e0 < E) ? e0 : E;  // E = no expert
+        ev[r] = e;
+        const unsigned peers = __match_any_sync(kFullMask, e);
+        const int before = e < E ? row[e] : 0;
+        __syncwarp();
+        if (e < E && lane == __ffs(peers) - 1) row[e] = before + __popc(peers);
+        __syncwarp();
+        rank[r] = before + __popc(peers & lanemask_lt());
+    }
+    bad = __syncthreads_or(bad);
+
+    // 3. warp counts -> warp bases within the CTA; the CTA's histogram
+    for (int e = threadIdx.x; e < E; e += kClThreads) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < kClWarps; ++w) {
+            const int c = wh[w * E + e];
+            wh[w * E + e] = run;
+            run += c;
+        }
+        hist[e] = run;
+    }
+    if (threadIdx.x == 0) hist[E] = bad;
+
+    // 4. every CTA's histogram is visible to the cluster; totals and this
+    //    CTA's base from all of them, plus the error flags
+    cluster_arrive();
+    cluster_wait();
+    const int cap = a.cap, masked = a.masked;
+    int flags = 0;
+    for (int e = threadIdx.x; e < E; e += kClThreads) {
+        int t = 0, b = 0;
+        for (unsigned c = 0; c < csize; c += 4) {
+            int v[4];
+            ld_peers4(hist + e, c, csize, v);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                t += v[j];
+                b += c + j < crank ? v[j] : 0;
+            }
+        }
+        tot[e] = t;
+        base[e] = b;
+        if (masked && t > cap) flags |= 2;
+    }
+    if (threadIdx.x < csize) {
+        int v[4];
+        ld_peers4(hist + E, threadIdx.x, threadIdx.x + 1, v);  // peer threadIdx.x's flag
+        if (v[0]) flags |= 1;
+    }
+    // done reading the peers (nothing to publish: relaxed); they may exit
+    // once every thread of the cluster has arrived here
+    cluster_arrive_relaxed();
+    if (flags) atomicOr(&s_flags, flags);
+
+    // 5. offsets: e*cap (masked) or the padded exclusive scan (contiguous)
+    const int align = a.align;
+    if (masked) {
+        for (int e = threadIdx.x; e <= E; e += kClThreads) off[e] = e * cap;
+        __syncthreads();
+    } else {
+        __syncthreads();
+        block_exclusive_scan<kClThreads>(
+            E, [&](int e) { return round_up_pow2(tot[e], align); }, off, scan_tmp);
+    }
+
+    if (writer) {
+        // 6. stable slots of this warp's entries
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+            const int i = w0 + r * 32 + lane;
+            if (i < w1) {
+                const int e = ev[r];
+                int dst = -1;
+                if (e < E) {
+                    const int slot = base[e] + row[e] + rank[r];
+                    if (!(masked && slot >= cap)) dst = off[e] + slot;
+                }
+                a.dst_row[i] = dst;
+                if (dst >= 0 && a.row_src) a.row_src[dst] = i;
+            }
+        }
+        // 7. counts and offsets, a slice of the experts per CTA; the status
+        //    word from CTA 0, the rank rows from the last CTA
+        for (int e = (int)crank * kClThreads + threadIdx.x; e < E; e += (int)csize * kClThreads) {
+            a.count[e] = tot[e];
+            a.offset[e] = off[e];
+        }
+        if (crank == 0 && threadIdx.x == 0) {
+            const int f = s_flags;
+            *a.status = (f & 1) ? EP_ERR_BAD_EXPERT_ID : (f & 2) ? EP_ERR_CAPACITY : EP_OK;
+        }
+        if (crank == csize - 1) {
+            if (threadIdx.x == 0) a.offset[E] = off[E];
+            if (a.rank_rows) {  // one warp per rank: sum of its experts' counts
+                const int per = E / a.R;
+                for (int rr = warp; rr < a.R; rr += kClWarps) {
+                    int sum = 0;
+                    for (int e = rr * per + lane; e < (rr + 1) * per; e += 32) sum += tot[e];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFullMask, sum, o);
+                    if (lane == 0) a.rank_rows[rr] = sum;
+                }
+            }
+        }
+    }
+
+    // 8. row_src = -1 on padding rows (contiguous) and empty slots (masked),
+    //    one warp per expert across all clusters
+    if (a.row_src) {
+        const int gw = (int)blockIdx.x * kClWarps + warp, nw = (int)gridDim.x * kClWarps;
+        for (int e = gw; e < E; e += nw) {
+            const int r0 = off[e] + (masked ? min(tot[e], cap) : tot[e]);
+            const int r1 = masked ? off[e] + cap : off[e + 1];
+            fill_minus_one(a.row_src, r0, r1, lane);
+        }
+    }
+    // no CTA leaves while a peer may still read its histogram
+    cluster_wait();
+}
+
+// Dynamic shared memory of the layout body: per-warp counts, the CTA's
+// histogram (+ bad-id flag), totals, bases and offsets.
+inline size_t cluster_smem(int E) {
+    return sizeof(int32_t) * ((size_t)kClWarps * E + 4 * (size_t)E + 2);
+}
+
+// CTAs of one cluster for TK entries with at most max_ctas per cluster, and
+// the entries per warp (32 x a power-of-two number of rounds).
+inline void cluster_shape(long long TK, int max_ctas, int *ctas, int *chunk) {
+    long long c = (TK + kClTargetPerCta - 1) / kClTargetPerCta;
+    if (c < 1) c = 1;
+    if (c > max_ctas) c = max_ctas;
+    int rounds = 1;
+    while ((long long)rounds * 32 * kClWarps * c < TK) rounds *= 2;
+    // as few CTAs as the rounds allow (fewer peers to read)
+    while (c > 1 && (long long)rounds * 32 * kClWarps * (c - 1) >= TK) --c;
+    *ctas = (int)c;
+    *chunk = 32 * rounds;
+}
+
+// Clusters needed for the row_src fill: one, or two to share a large masked
+// fill (the fill is bound by each SM's store rate, about 30 bytes per clock;
+// more than two clusters measured slower at the DeepSeek-V3 decode shape).
+inline int fill_clusters(const ep_layout_t &L, int ctas) {
+    if (L.kind != EP_LAYOUT_MASKED || L.row_src == nullptr) return 1;
+    const long long rows = (long long)L.num_experts * L.capacity;
+    return rows > (long long)ctas * 2048 ? 2 : 1;
+}
+
+// The layout body's arguments for layout L.
+inline ClusterArgs cluster_args(const int32_t *topk_idx, const ep_layout_t &L, int chunk) {
+    ClusterArgs c;
+    c.idx = topk_idx;
+    c.TK = L.num_tokens * L.num_topk;
+    c.E = L.num_experts;
+    c.R = L.num_ranks;
+    c.masked = L.kind == EP_LAYOUT_MASKED;
+    c.align = c.masked ? 1 : L.align;
+    c.cap = c.masked ? L.capacity : 0;
+    c.chunk = chunk;
+    c.dst_row = L.dst_row;
+    c.row_src = L.row_src;
+    c.count = L.expert_count;
+    c.offset = L.expert_offset;
+    c.rank_rows = L.rank_rows;
+    c.status = L.status;
+    return c;
+}
+
+// Largest cluster (16 CTAs, else the portable 8) that the device can
+// co-schedule for kernel `func` of kClThreads threads and `smem` bytes of
+// dynamic shared memory; once per device and kernel.  Sets the kernel's
+// dynamic shared-memory limit and non-portable-cluster attribute.
+int max_cluster_ctas(const void *func, size_t smem);
+
+// Launch `func(args...)` as `clusters` clusters of `ctas` CTAs of kClThreads
+// threads, optionally as a programmatic dependent of the previous kernel.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_clusters(void (*func)(KArgs...), int ctas, int clusters, size_t smem,
+                            cudaStream_t stream, bool programmatic, Args... args) {
+    cudaError_t err = allow_dynamic_smem(func, smem);
+    if (err != cudaSuccess) return err;
+    if (ctas > 8) {
+        err = cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas * clusters);
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, func, static_cast<KArgs>(args)...);
+}
+
+}  // namespace cl
+}  // namespace ep

@@ -544,144 +544,6 @@ __global__ void __launch_bounds__(512)
     for (int i = 1; i < n; ++i) token(i, false);
 }
 
-// ---- the layout and the dispatch of a decode-sized batch in one kernel ----
-
-struct FusedArgs {
-    const int32_t *idx;
-    const uint16_t *x;
-    int T, K, E, H, R, masked, align, cap;
-    int per;  // tokens per CTA (CTA c takes [c*per, min(T, (c+1)*per)))
-    int32_t *dst_row, *row_src, *count, *offset, *rank_rows, *status;
-    uint8_t *out;
-    uint32_t *scales;
-    const float *topk_w;
-    float *row_w;
-    int mn_stride, mn_cap;
-};
-
-constexpr int kFusedThreads = 512;
-constexpr int kFusedMaxEntries = 8192;  // T*K up to here: one kernel
-
-// Every CTA recounts all entries (expert totals, and the entries before its
-// tokens), derives the offsets itself, ranks its own entries in (token, k)
-// order with one warp, writes its part of the layout arrays (CTA 0 the
-// counts, offsets, rank rows and status; expert e's empty rows the CTA
-// e % gridDim.x), and then dispatches its tokens as direct_kernel does.
-template <int Q>
-__global__ void __launch_bounds__(kFusedThreads) fused_kernel(FusedArgs f) {
-    constexpr int NT = kFusedThreads, kWarps = NT / 32;
-    constexpr bool kFp8 = Q != EP_QUANT_NONE;
-    extern __shared__ int32_t fsm[];
-    const int E = f.E, K = f.K, H = f.H;
-    int32_t *tot = fsm;           // [E] expert totals
-    int32_t *run = tot + E;       // [E] entries before this CTA's tokens, then running slots
-    int32_t *off = run + E;       // [E+1] first row of each expert
-    int32_t *sdst = off + E + 1;  // [per*K] destinations of this CTA's entries
-    __shared__ int32_t scan_tmp[kWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t0 = blockIdx.x * f.per, t1 = min(f.T, t0 + f.per);
-    const int i0 = t0 * K, i1 = t1 * K;
-    const int slots = kFp8 ? (H >> 7) * 8 : H / 8;
-
-    // The previous kernel may have produced topk_idx and x, and may still read
-    // the layout arrays: wait for it before anything else (a no-op for the
-    // ordinary launch used now); then the next kernel may launch.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // the first token's slot is in flight during the layout work below
-    uint4 ca = make_uint4(0, 0, 0, 0), cb = ca, na = ca, nb = ca;
-    const bool first_slot = (int)threadIdx.x < slots;
-    if (t0 < t1 && first_slot) load_slot<Q>(f.x + (size_t)t0 * H, threadIdx.x, ca, cb);
-
-    // 1. expert totals and the entries before this CTA's tokens
-    for (int e = threadIdx.x; e < E; e += NT) tot[e] = run[e] = 0;
-    __syncthreads();
-    const int bad = __syncthreads_or(count_all<NT>(f.idx, f.T * K, E, i0, tot, run));
-    int over = 0;
-    if (f.masked)
-        for (int e = threadIdx.x; e < E; e += NT) over |= tot[e] > f.cap;
-    over = __syncthreads_or(over);
-
-    // 2. offsets: e*cap (masked) or the padded exclusive scan (contiguous)
-    if (f.masked) {
-        for (int e = threadIdx.x; e <= E; e += NT) off[e] = e * f.cap;
-        __syncthreads();
-    } else {
-        const int align = f.align;
-        block_exclusive_scan<NT>(
-            E, [&](int e) { return (tot[e] + align - 1) & ~(align - 1); }, off, scan_tmp);
-    }
-    if (blockIdx.x == 0) {
-        if (threadIdx.x == 0)
-            *f.status = bad ? EP_ERR_BAD_EXPERT_ID : over ? EP_ERR_CAPACITY : EP_OK;
-        for (int e = threadIdx.x; e < E; e += NT) {
-            f.count[e] = tot[e];
-            f.offset[e] = off[e];
-        }
-        if (threadIdx.x == 0) f.offset[E] = off[E];
-        if (f.rank_rows) {  // one warp per rank: sum of its experts' counts
-            const int per_rank = E / f.R;
-            for (int r = warp; r < f.R; r += kWarps) {
-                int sum = 0;
-                for (int e = r * per_rank + lane; e < (r + 1) * per_rank; e += 32) sum += tot[e];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFullMask, sum, o);
-                if (lane == 0) f.rank_rows[r] = sum;
-            }
-        }
-    }
-
-    // 3. stable slots of this CTA's entries: 32 at a time in (token, k) order
-    if (warp == 0) {
-        for (int b = i0; b < i1; b += 32) {
-            const int i = b + lane;
-            const int e = i < i1 ? __ldg(f.idx + i) : -1;
-            const bool valid = e >= 0 && e < E;
-            const unsigned peers = __match_any_sync(kFullMask, valid ? e : E);
-            const int slot = valid ? run[e] + __popc(peers & lanemask_lt()) : 0;
-            __syncwarp();
-            if (valid && lane == __ffs(peers) - 1) run[e] += __popc(peers);
-            __syncwarp();
-            if (i < i1) {
-                const int d = valid && !(f.masked && slot >= f.cap) ? off[e] + slot : -1;
-                f.dst_row[i] = d;
-                if (d >= 0 && f.row_src) f.row_src[d] = i;
-                sdst[i - i0] = d;
-            }
-        }
-    }
-    // 4. row_src = -1 on padding rows (contiguous) and empty slots (masked)
-    if (f.row_src) {
-        for (int e = blockIdx.x + (int)gridDim.x * warp; e < E; e += (int)gridDim.x * kWarps) {
-            const int r0 = off[e] + (f.masked ? min(tot[e], f.cap) : tot[e]);
-            const int r1 = f.masked ? off[e] + f.cap : off[e + 1];
-            for (int r = r0 + lane; r < r1; r += 32) f.row_src[r] = -1;
-        }
-    }
-    __syncthreads();
-
-    // 5. dispatch this CTA's tokens (as direct_kernel, destinations from sdst)
-    const bool weights = f.row_w != nullptr && (int)threadIdx.x < K;
-    int cd = t0 < t1 && lane < K ? sdst[lane] : -1;
-    float cw = t0 < t1 && weights ? __ldg(f.topk_w + (size_t)t0 * K + lane) : 0.0f;
-    for (int t = t0; t < t1; ++t) {
-        int nd = -1;
-        float nw = 0.0f;
-        if (t + 1 < t1) {  // the next token, in flight meanwhile
-            if (first_slot) load_slot<Q>(f.x + (size_t)(t + 1) * H, threadIdx.x, na, nb);
-            if (lane < K) nd = sdst[(t + 1 - t0) * K + lane];
-            if (weights) nw = __ldg(f.topk_w + (size_t)(t + 1) * K + lane);
-        }
-        store_token<Q>(f.x, t, H, K, ca, cb, false, ca, 0, cd, f.out, f.scales, f.mn_stride,
-                       f.mn_cap);
-        if (weights && cd >= 0) f.row_w[cd] = cw;
-        ca = na;
-        cb = nb;
-        cd = nd;
-        cw = nw;
-    }
-}
-
 // bf16 dispatch: one warp; lane 0 drives the TMA, lanes k < K hold the
 // destinations.  Token i uses stage i % stages; a stage is refilled once the
 // stores of its token have read it.
@@ -874,43 +736,6 @@ cudaError_t launch_copy(const ep_layout_t &L, const void *x, int H, void *out_ro
                          xstage_bytes);
 }
 
-template <int Q>
-cudaError_t launch_fused(const int32_t *topk_idx, const ep_layout_t &L, const void *x, int H,
-                         void *out_rows, void *out_scales, const float *topk_w, float *row_w,
-                         cudaStream_t stream) {
-    FusedArgs f;
-    f.idx = topk_idx;
-    f.x = static_cast<const uint16_t *>(x);
-    f.T = L.num_tokens;
-    f.K = L.num_topk;
-    f.E = L.num_experts;
-    f.H = H;
-    f.R = L.num_ranks;
-    f.masked = L.kind == EP_LAYOUT_MASKED;
-    f.align = f.masked ? 1 : L.align;
-    f.cap = f.masked ? L.capacity : 0;
-    f.per = (f.T + sm_count() - 1) / sm_count();  // one CTA per SM at most
-    f.dst_row = L.dst_row;
-    f.row_src = L.row_src;
-    f.count = L.expert_count;
-    f.offset = L.expert_offset;
-    f.rank_rows = L.rank_rows;
-    f.status = L.status;
-    f.out = static_cast<uint8_t *>(out_rows);
-    f.scales = static_cast<uint32_t *>(out_scales);
-    f.topk_w = topk_w;
-    f.row_w = row_w;
-    f.mn_stride = mn_layout(L, f.mn_cap);
-    const int grid = (f.T + f.per - 1) / f.per;
-    const size_t smem = sizeof(int32_t) * (3 * (size_t)f.E + 1 + (size_t)f.per * f.K);
-    cudaError_t err = allow_dynamic_smem(fused_kernel<Q>, smem);
-    if (err != cudaSuccess) return err;
-    // an ordinary launch: launched early, its large CTAs would sit on the SMs
-    // in griddepcontrol.wait and take registers from the previous kernel
-    // (measured: a combine before it ran slower by more than the overlap won)
-    return launch_kernel(fused_kernel<Q>, grid, kFusedThreads, smem, stream, false, f);
-}
-
 }  // namespace
 
 cudaError_t launch_dispatch(const ep_layout_t &L, const void *x, int H, ep_quant_t quant,
@@ -953,24 +778,15 @@ cudaError_t launch_layout_dispatch(const int32_t *topk_idx, const ep_layout_t &L
                                    int32_t *workspace, const void *x, int H, ep_quant_t quant,
                                    void *out_rows, void *out_scales, const float *topk_w,
                                    float *row_w, cudaStream_t stream) {
-    const long long TK = (long long)L.num_tokens * L.num_topk;
-    if (L.num_tokens == 0 || TK > kFusedMaxEntries) {  // the two separate steps
-        cudaError_t err = launch_layout(topk_idx, L, workspace, stream);
-        if (err != cudaSuccess) return err;
-        return launch_dispatch(L, x, H, quant, out_rows, out_scales, topk_w, row_w, stream);
-    }
-    switch (quant) {
-        case EP_QUANT_NONE:
-            return launch_fused<EP_QUANT_NONE>(topk_idx, L, x, H, out_rows, out_scales, topk_w, row_w, stream);
-        case EP_QUANT_FP8_F32:
-            return launch_fused<EP_QUANT_FP8_F32>(topk_idx, L, x, H, out_rows, out_scales, topk_w, row_w, stream);
-        case EP_QUANT_MXFP8:
-            return launch_fused<EP_QUANT_MXFP8>(topk_idx, L, x, H, out_rows, out_scales, topk_w, row_w, stream);
-        case EP_QUANT_FP8_UE8M0_MN:
-            return launch_fused<EP_QUANT_FP8_UE8M0_MN>(topk_idx, L, x, H, out_rows, out_scales, topk_w, row_w, stream);
-        default:
-            return launch_fused<EP_QUANT_FP8_UE8M0>(topk_idx, L, x, H, out_rows, out_scales, topk_w, row_w, stream);
-    }
+    // The layout and the dispatch back to back; the dispatch is a programmatic
+    // dependent of the layout, so its first rows load and quantise while the
+    // layout runs.  One kernel doing both (every cluster computing the layout,
+    // each CTA dispatching its slice's tokens from shared-memory destinations;
+    // or every CTA recounting all entries) measured no faster at the decode
+    // shapes.
+    const cudaError_t err = launch_layout(topk_idx, L, workspace, stream);
+    if (err != cudaSuccess) return err;
+    return launch_dispatch(L, x, H, quant, out_rows, out_scales, topk_w, row_w, stream);
 }
 
 }  // namespace ep

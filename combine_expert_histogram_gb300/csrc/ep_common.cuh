@@ -133,36 +133,6 @@ __device__ __forceinline__ void block_exclusive_scan(int n, F value, int32_t *ou
     __syncthreads();
 }
 
-// Expert totals (and, when pre != nullptr, the entries before `start`) of
-// the first TK entries, by shared-memory atomics; loads are issued eight at a
-// time ahead of their atomics.  Returns 1 if this thread saw an id outside
-// [-1, E).
-template <int NT>
-__device__ __forceinline__ int count_all(const int32_t *__restrict__ idx, int TK, int E, int start,
-                                         int32_t *tot, int32_t *pre) {
-    constexpr int kBatchLoads = 8;
-    int bad = 0;
-    for (int i0 = threadIdx.x; i0 < TK; i0 += NT * kBatchLoads) {
-        int ev[kBatchLoads];
-#pragma unroll
-        for (int u = 0; u < kBatchLoads; ++u) {
-            const int i = i0 + u * NT;
-            ev[u] = i < TK ? __ldg(idx + i) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatchLoads; ++u) {
-            const int i = i0 + u * NT, e = ev[u];
-            if (e >= 0 && e < E) {
-                atomicAdd(&tot[e], 1);
-                if (pre && i < start) atomicAdd(&pre[e], 1);
-            } else if (e != -1 && i < TK) {
-                bad = 1;
-            }
-        }
-    }
-    return bad;
-}
-
 // Per-device properties, cached on first use (host side).
 int sm_count();
 
@@ -208,9 +178,7 @@ struct LayoutPlan {
     int tile;         // entries per tile
     int grid;         // CTAs of the assign kernel (>= tiles; extra CTAs fill padding)
     size_t smem;      // dynamic shared memory of the assign kernel
-    size_t ws_bytes;  // scratch: tiles x E int32 per-tile histograms (0 when tiles == 1
-                      // or self_hist)
-    bool self_hist;   // several tiles, one kernel: every CTA recounts all entries itself
+    size_t ws_bytes;  // scratch: tiles x E int32 per-tile histograms (0 for the cluster kernel)
     bool cluster;     // decode-sized: one kernel of one thread-block cluster (tiles = its CTAs,
                       // for the largest cluster; the launch may use fewer, larger slices)
 };
@@ -222,7 +190,7 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
 
 // One CTA waiting on a barrier nothing completes, for at most limit_clocks.
 cudaError_t launch_wait_selftest(int32_t *status, long long limit_clocks, cudaStream_t stream);
-// ep_layout followed by ep_dispatch; one kernel for decode-sized batches.
+// ep_layout followed by ep_dispatch, launched back to back.
 cudaError_t launch_layout_dispatch(const int32_t *topk_idx, const ep_layout_t &L,
                                    int32_t *workspace, const void *x, int H, ep_quant_t quant,
                                    void *out_rows, void *out_scales, const float *topk_w,

@@ -244,9 +244,9 @@ ep_status_t ep_dispatch(const ep_layout_t *layout, const void *x, int32_t hidden
  * dispatch).  Arguments, outputs and errors are exactly those of the two
  * calls (topk_idx, layout and workspace as for ep_layout; x, hidden, quant,
  * out_rows, out_scales, topk_w, row_w as for ep_dispatch), and the results
- * are bit-identical to them.  Up to 8192 entries (T*K) one kernel does both
- * (no workspace is read then: each CTA recounts the entries itself); larger
- * batches run the two steps back to back.
+ * are bit-identical to them.  The two kernels are launched back to back, the
+ * dispatch as a programmatic dependent of the layout (its first rows load
+ * and quantise while the layout runs).
  */
 ep_status_t ep_layout_dispatch(const int32_t *topk_idx, const ep_layout_t *layout,
                                void *workspace, size_t workspace_bytes, const void *x,

@@ -26,7 +26,7 @@ def _guards_intact(buf, n):
     return bool((buf[:GUARD] == PAT).all()) and bool((buf[GUARD + n:] == PAT).all())
 
 
-# one tile; several tiles in one kernel; a histogram kernel + assign kernel
+# cluster kernel of 1, 8 and 16 CTAs (4 rounds per warp); histogram + assign kernels
 @pytest.mark.parametrize("T", [50, 500, 3000, 5000])
 def test_bad_expert_ids_raise_status_without_stray_writes(T):
     E, K = 16, 4
@@ -94,7 +94,7 @@ def test_status_resets_on_next_layout():
     assert int(L.status.item()) == 0
 
 
-@pytest.mark.parametrize("T", [300, 3000])  # several tiles: one kernel; two kernels
+@pytest.mark.parametrize("T", [300, 3000])  # cluster kernel; histogram + assign kernels
 def test_multi_tile_status_max_and_reset(T):
     """Bad ids and an over-full masked expert together report the larger code;
     the next layout of good ids resets it."""
@@ -116,8 +116,8 @@ def test_multi_tile_status_max_and_reset(T):
     assert int(L2.status.item()) == 0
 
 
-# one CTA; tiles in one kernel; histogram kernel + assign kernel
-@pytest.mark.parametrize("cap", [64, 800, 2500])
+# cluster kernel of 1-2 and 13 CTAs; histogram + assign kernels
+@pytest.mark.parametrize("cap", [64, 800, 5000])
 def test_masked_capacity_exact_boundary(cap):
     """An expert receiving exactly `capacity` rows is fine; one row more raises
     EP_ERR_CAPACITY and only the extra entry goes unplaced."""

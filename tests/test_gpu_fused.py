@@ -1,6 +1,7 @@
 """ep_layout_dispatch: the layout and the dispatch in one call must give
 bit-identical results to ep_layout followed by ep_dispatch, and match the
-oracle, for decode-sized batches (one kernel) and beyond (two steps)."""
+oracle, on both layout paths (the cluster kernel up to 16384 entries, the
+histogram + assign kernels beyond)."""
 import numpy as np
 import pytest
 import torch
@@ -28,8 +29,12 @@ CASES = [
       quant="fp8_f32", align=16, seed=83),
     W("fused_bf16_big_h", T=40, H=16384, E=8, K=2, routing="softmax", layout="masked",
       quant="none", cap=40, seed=84),
-    W("two_steps", T=2000, H=512, E=64, K=8, routing="softmax", layout="contig",
-      quant="fp8_ue8m0", align=128, seed=85),   # 16000 entries: ep_layout + ep_dispatch
+    W("cluster_16000", T=2000, H=512, E=64, K=8, routing="softmax", layout="contig",
+      quant="fp8_ue8m0", align=128, seed=85),   # 16000 entries: cluster layout of 4 rounds
+    W("cluster_bad_over", T=900, H=512, E=64, K=8, routing="softmax", layout="masked",
+      quant="fp8_ue8m0", cap=60, R=4, seed=86),  # bad ids and capacity overflow
+    W("tiled_16800", T=2100, H=256, E=64, K=8, routing="softmax", layout="contig",
+      quant="fp8_f32", align=128, seed=87),     # 16800 entries: histogram + assign kernels
 ]
 
 
@@ -59,9 +64,10 @@ def _arrays(L):
 def test_fused_equals_two_calls_and_oracle(w):
     case = gh.make_case(w)
     idx = case["idx"].copy()
-    if w.name == "fused_f32_ragged":  # unrouted entries and a bad id too
+    if w.name in ("fused_f32_ragged", "cluster_bad_over"):  # unrouted entries and bad ids too
         idx[::7, 3] = -1
         idx[5, 0] = w.E + 2
+        idx[w.T - 1, w.K - 1] = -9
     idx_d = torch.from_numpy(idx).cuda()
     case["idx"], case["idx_d"] = idx, idx_d
     # reference: the two calls
@@ -137,7 +143,7 @@ QUANTS = ["none", "fp8_f32", "fp8_ue8m0", "mxfp8", "fp8_ue8m0_mn"]
 
 @pytest.mark.parametrize("seed", range(24))
 def test_fused_fuzz_equals_two_calls(seed):
-    """Random decode-sized shapes (up to 8192 entries, so one kernel) with -1
+    """Random decode-sized shapes (up to 8192 entries) with -1
     ids, repeated experts and small masked capacities: every output array
     equals ep_layout followed by ep_dispatch, and the one call's outputs equal
     the oracle's."""

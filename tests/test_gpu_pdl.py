@@ -4,7 +4,7 @@ still runs must read that predecessor's results only after waiting for it.
 The layout, dispatch, combine and rank kernels are launched as programmatic
 dependents (the layout's first kernel waits for its predecessor before
 anything else), and dispatch and combine let their dependents launch at their
-start; the one-call layout + dispatch kernel is an ordinary launch.  Here the stream is first held behind a long fill, so that the
+start.  Here the stream is first held behind a long fill, so that the
 library's launches queue back to back and every programmatic edge is live
 (dispatch starts while the layout runs, combine while dispatch runs, the next
 step's layout while combine runs).
