@@ -34,6 +34,8 @@
 //     (token, k) order;
 //   * extra CTAs (masked layouts with row_src) only count the experts with
 //     shared-memory atomics and write -1 into row_src for empty slots.
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "cluster_layout.cuh"
@@ -332,6 +334,19 @@ ClusterKernel cluster_kernel(int rounds) {
 
 namespace cl {
 
+// EP_MAX_CLUSTER_CTAS=8 caps the cluster at the portable size (for a device
+// partition that cannot place 16 co-scheduled CTAs, or to check that
+// configuration); values below 8 count as 8, since the kernel's rounds per
+// warp allow at most 8 x 8 x 256 entries on 8 CTAs.
+int cluster_ctas_cap() {
+    static const int cap = [] {
+        const char *v = getenv("EP_MAX_CLUSTER_CTAS");
+        const int n = v ? atoi(v) : kClMaxCtas;
+        return n < 8 ? 8 : n > kClMaxCtas ? kClMaxCtas : n;
+    }();
+    return cap;
+}
+
 int max_cluster_ctas(const void *func, size_t smem) {
     struct Entry {
         const void *func;
@@ -372,6 +387,7 @@ int max_cluster_ctas(const void *func, size_t smem) {
             best = kClMaxCtas;
     }
     cudaGetLastError();  // a refused query leaves no error behind
+    if (best > cluster_ctas_cap()) best = cluster_ctas_cap();
     if (used < 32) cache[used++] = Entry{func, dev, smem, best};
     return best;
 }

@@ -193,6 +193,12 @@ size_t ep_layout_workspace_bytes(const ep_layout_t *layout);
  *                      masked slots >= capacity (EP_ERR_CAPACITY raised)
  *   row_src[dst_row[i]] = i; every other row of the row space = -1
  *   rank_rows[r]     = sum of expert_count over rank r's experts
+ *
+ * Up to 16384 entries (T*K) one kernel of one thread-block cluster computes
+ * the layout and no workspace is needed; its cluster has 16 CTAs where the
+ * device can co-schedule them, else 8.  The environment variable
+ * EP_MAX_CLUSTER_CTAS=8 (read once per process) caps it at 8, for a device
+ * partition that cannot place 16 co-scheduled CTAs.
  */
 ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *layout, void *workspace,
                       size_t workspace_bytes, ep_stream_t stream);

@@ -82,6 +82,13 @@ MID = [
                        layout="contig", quant="fp8_ue8m0", align=128, seed=19),
     workloads.Workload("smem48k_layout", T=128, H=256, E=361, K=8, routing="softmax",
                        layout="contig", quant="fp8_f32", align=1, seed=20),
+    # the cluster layout at its limits: K=32 (16000 entries, 16 CTAs x 4
+    # rounds per warp) and E=1024 (just over 48 KB of shared memory) with a
+    # masked capacity that overflows
+    workloads.Workload("cluster_k32", T=500, H=256, E=256, K=32, routing="softmax",
+                       layout="contig", quant="fp8_f32", align=64, seed=21),
+    workloads.Workload("cluster_e1024", T=2000, H=128, E=1024, K=8, routing="zipf",
+                       layout="masked", quant="fp8_ue8m0", cap=64, R=16, seed=22),
     # > 128 tiles of 2048 entries: tiles of several passes
     workloads.Workload("multipass", T=40000, H=128, E=64, K=8, routing="softmax",
                        layout="contig", quant="fp8_ue8m0", align=128, R=4, seed=10),
