@@ -11,9 +11,11 @@
 //   * the T*K entries are cut into tiles; warp w of a tile's CTA owns a
 //     contiguous chunk of at most 256 entries, lane l holds entries
 //     chunk + 32r + l in registers (all loads issued up front);
-//   * lanes holding the same expert in a round find each other with
-//     ceil(log2(E+1)) independent __ballot_sync's (one per bit of the id);
-//     the mask is kept per round and reused for ranking;
+//   * lanes holding the same expert in a round find each other with one
+//     __match_any_sync (it measured 601 k -> 384 k warp instructions and
+//     14.0 -> 11.4 us for the assign kernel of 65536 entries against one
+//     __ballot_sync per bit of the id); the mask is kept per round and
+//     reused for ranking;
 //   * up to 16384 entries (decode-sized batches) one kernel of one
 //     thread-block cluster does everything (cluster_layout_kernel, its body
 //     in cluster_layout.cuh): each
@@ -71,7 +73,7 @@ __device__ __forceinline__ void fetch_chunk(const int32_t *__restrict__ idx, int
 }
 
 // Map invalid ids to E (recording bad ones) and find each round's peers.
-__device__ __forceinline__ void classify_chunk(int c0, int c1, int E, int nbits, Chunk &c) {
+__device__ __forceinline__ void classify_chunk(int c0, int c1, int E, Chunk &c) {
     c.bad = 0;
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
@@ -82,28 +84,17 @@ __device__ __forceinline__ void classify_chunk(int c0, int c1, int E, int nbits,
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
         unsigned m = 0;
-        if (c0 + r * 32 < c1) {  // warp-uniform: rounds past the chunk stay empty
-            const int v = c.ev[r];
-            m = kFullMask;
-#pragma unroll 1
-            for (int b = 0; b < nbits; ++b) {  // warp-uniform trip count; kept rolled (code size)
-                const unsigned bit = (v >> b) & 1u;
-                const unsigned bal = __ballot_sync(kFullMask, bit);
-                m &= bit ? bal : ~bal;
-            }
-        }
+        if (c0 + r * 32 < c1)  // warp-uniform: rounds past the chunk stay empty
+            m = __match_any_sync(kFullMask, c.ev[r]);
         c.peers[r] = m;
     }
 }
 
 __device__ __forceinline__ void load_chunk(const int32_t *__restrict__ idx, int c0, int c1,
-                                           int E, int nbits, Chunk &c) {
+                                           int E, Chunk &c) {
     fetch_chunk(idx, c0, c1, c);
-    classify_chunk(c0, c1, E, nbits, c);
+    classify_chunk(c0, c1, E, c);
 }
-
-
-__device__ __forceinline__ int id_bits(int E) { return 32 - __clz(E); }  // E itself must fit
 
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -166,7 +157,6 @@ __global__ void __launch_bounds__(kTileThreads) assign_kernel(AssignArgs a) {
     const int tile_id = blockIdx.x;
     const int start = tile_id * a.tile;
     const int end = min(a.TK, start + a.tile);
-    const int nbits = id_bits(E);
     const int pass_len = kWarps * a.chunk;
 
     if (!assigns) {
@@ -199,9 +189,9 @@ __global__ void __launch_bounds__(kTileThreads) assign_kernel(AssignArgs a) {
         const int c0 = start + p * pass_len + warp * a.chunk;
         const int c1 = min(end, c0 + a.chunk);
         if (passes == 1)
-            classify_chunk(c0, c1, E, nbits, c);
+            classify_chunk(c0, c1, E, c);
         else
-            load_chunk(a.idx, c0, c1, E, nbits, c);
+            load_chunk(a.idx, c0, c1, E, c);
         int32_t *row = wh + (p * kWarps + warp) * E;
 #pragma unroll
         for (int r = 0; r < kRounds; ++r) {
@@ -266,7 +256,7 @@ __global__ void __launch_bounds__(kTileThreads) assign_kernel(AssignArgs a) {
     for (int p = 0; p < passes; ++p) {
         const int c0 = start + p * pass_len + warp * a.chunk;
         const int c1 = min(end, c0 + a.chunk);
-        if (passes > 1) load_chunk(a.idx, c0, c1, E, nbits, c);
+        if (passes > 1) load_chunk(a.idx, c0, c1, E, c);
         int32_t *row = wh + (p * kWarps + warp) * E;
 #pragma unroll
         for (int r = 0; r < kRounds; ++r) {
