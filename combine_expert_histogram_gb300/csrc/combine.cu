@@ -7,9 +7,13 @@
 // with fp32 products and sums each rounded separately (no fused multiply-add),
 // starting from +0.  The products come two at a time from packed f32x2
 // multiplies (each lane an IEEE round-to-nearest multiply); the sums stay
-// scalar __fadd_rn: with a packed add consuming a packed product, the compiler
-// was measured to contract the pair into a fused multiply-add (results then
-// differ from separate rounding in cancelling sums).
+// scalar __fadd_rn: with a packed add consuming a packed product, the pair is
+// contracted into a fused multiply-add (results then differ from separate
+// rounding in cancelling sums).  Measured on GB300: the contraction happens
+// in the assembler, for packed `add.rn.f32x2` after `mul.rn.f32x2` written
+// as inline PTX with explicit rounding, after an `fma.rn.f32x2` with a -0
+// addend, and with --fmad=false (each packed operation alone was exact; the
+// chain differed from the scalar one in 43 % of 2 M random pairs).
 //
 // HBM-bound gather: one lane owns 8 output elements (16 bytes) of one token
 // -- 16 elements with one 256-bit load per row when the batch fills the GPU
