@@ -66,3 +66,49 @@ def test_graph_replay_matches_oracle(name):
         ref = gh.check_layout(wi, case, res)
         gh.check_dispatch(wi, case, res, ref, sample_tokens=512, check_row_w=False)
         assert gh.check_combine(wi, case, res, ref, sample_tokens=512) == 1.0
+
+
+FIRST_CALL_IN_CAPTURE = """
+import sys
+sys.path.insert(0, {root!r})
+import numpy as np
+import torch
+import oracle
+import workloads
+from combine_expert_histogram_gb300 import binding as ep
+from tests import gpu_harness as gh
+for name in ("qwen3_30b_a3b_decode", "dsv3_prefill"):
+    w = workloads.CONFIGS[name]
+    if name == "dsv3_prefill":
+        w = w.with_(T=4096, name="dsv3_prefill_T4096")   # the tiled layout path
+    case = gh.make_case(w)
+    L = ep.new_layout(w.T, w.K, w.E, w.layout, align=w.align, capacity=w.cap, num_ranks=w.R)
+    rows = torch.empty((L.rows_capacity, w.H), dtype=torch.uint8, device="cuda")
+    sc = ep.scale_buffer(L, w.H, w.quant)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):  # the library's first launches of these kernels
+        ep.ep_layout(case["idx_d"], w.E, out=L, stream=s)
+        ep.ep_dispatch(L, case["x_d"], w.quant, out_rows=rows, out_scales=sc, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    res = dict(L=L, rows=L.rows_capacity, out_rows=rows, out_scales=sc, row_w=None)
+    ref = gh.check_layout(w, case, res)
+    gh.check_dispatch(w, case, res, ref, check_row_w=False)
+    print("ok", name)
+"""
+
+
+def test_first_library_call_inside_graph_capture():
+    """In a fresh process, the layout and dispatch kernels are first launched
+    while a CUDA graph is being captured (the per-device queries and kernel
+    attributes of the first launch happen inside the capture); the replayed
+    graph matches the oracle, on the cluster and on the tiled layout path."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", FIRST_CALL_IN_CAPTURE.format(root=root)], cwd=root,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.count("ok ") == 2
