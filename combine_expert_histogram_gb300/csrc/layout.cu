@@ -7,35 +7,32 @@
 // (ElasticBuffer) MoE A2A backend", section "Supported scope".
 //
 // Design (deterministic, no global atomics on slot order; latency-bound, so
-// the goal is short dependency chains and many warps):
-//   * the T*K entries are cut into tiles; warp w of a tile's CTA owns a
-//     contiguous chunk of at most 256 entries, lane l holds entries
-//     chunk + 32r + l in registers (all loads issued up front);
-//   * lanes holding the same expert in a round find each other with one
-//     __match_any_sync (it measured 601 k -> 384 k warp instructions and
-//     14.0 -> 11.4 us for the assign kernel of 65536 entries against one
-//     __ballot_sync per bit of the id); the mask is kept per round and
-//     reused for ranking;
-//   * up to 16384 entries (decode-sized batches) one kernel of one
-//     thread-block cluster does everything (cluster_layout_kernel, its body
-//     in cluster_layout.cuh): each
-//     CTA ranks its own slice of the entries (__match_any_sync peer masks,
-//     per-warp counts), publishes its expert histogram in shared memory, and
+// the goal is short dependency chains and many warps).  In both paths lanes
+// holding the same expert in a round of 32 entries find each other with one
+// __match_any_sync, and an entry's slot is the number of entries of its
+// expert before it: in lower CTAs or tiles, in lower warps, in earlier rounds
+// and in lower lanes -- exactly ascending (token, k) order.
+//
+//   * Up to 16384 entries (decode-sized batches): one kernel of one
+//     thread-block cluster (cluster_layout_kernel; its body is in
+//     cluster_layout.cuh).  Each CTA ranks its own slice of the entries with
+//     per-warp counts, publishes its expert histogram in shared memory, and
 //     after a cluster barrier reads its peers' histograms through distributed
 //     shared memory (four peers' loads in flight at once) for the expert
-//     totals and its slice's base; the CTAs share the row_src fill; no
-//     workspace, and no CTA reads more than its own slice of topk_idx;
-//   * beyond that, tile_hist_kernel counts each tile's experts (shared-memory
-//     atomics; counts need no order) into the scratch workspace [tiles][E],
-//     then assign_kernel (launched as a programmatic dependent, so its loads
-//     and ballots overlap tile_hist) waits for it and sums the workspace
-//     columns into the expert totals and its tile's base;
-//   * assign_kernel scans the padded counts, turns per-warp histograms into
-//     per-warp starting slots and gives each entry
-//     slot = warp base + #lower lanes with the same expert: exactly ascending
-//     (token, k) order;
-//   * extra CTAs (masked layouts with row_src) only count the experts with
-//     shared-memory atomics and write -1 into row_src for empty slots.
+//     totals and its slice's base.  No workspace, and no CTA reads more than
+//     its own slice of topk_idx; the CTAs share the row_src fill.
+//   * Beyond that: tile_hist_kernel counts each tile's experts (shared-memory
+//     atomics; counts need no order) into the workspace [tiles][E]; then
+//     assign_kernel, a programmatic dependent whose loads and match masks
+//     overlap tile_hist, waits for it, sums the workspace columns into the
+//     expert totals and its tile's base, scans the padded counts, turns
+//     per-warp histograms into per-warp starting slots and writes the slots.
+//     Warp w of a tile's CTA owns a contiguous chunk of up to 256 entries,
+//     lane l holding entries chunk + 32r + l in registers (all loads issued
+//     up front).  One __match_any_sync per round replaced one __ballot_sync
+//     per bit of the id (601 k -> 384 k warp instructions, 14.0 -> 11.4 us
+//     for 65536 entries).  Extra CTAs of masked layouts with row_src only
+//     sum the expert totals and write -1 into row_src for empty slots.
 #include <stdlib.h>
 
 #include <mutex>
