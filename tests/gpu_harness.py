@@ -93,13 +93,14 @@ def check_layout(w, case, g, orc=None):
 
 def check_dispatch(w, case, g, ref, sample_tokens=None, seed=0, orc=None, check_row_w=True,
                    check_empty=None):
-    """Bit-exact rows/scales/row_w; sentinel kept on rows the layout leaves empty."""
+    """Bit-exact rows/scales/row_w; sentinel kept on rows the layout leaves empty.
+    Returns the number of tokens whose rows were compared."""
     if check_empty is None:
         check_empty = check_row_w
     orc = orc or oracle.default()
     T, K = case["idx"].shape
     if T == 0:
-        return
+        return 0
     dst = ref["dst_row"]
     if sample_tokens is None or sample_tokens >= T:
         toks = np.arange(T)
@@ -110,7 +111,7 @@ def check_dispatch(w, case, g, ref, sample_tokens=None, seed=0, orc=None, check_
     for c0 in range(0, toks.size, CHUNK_TOKENS):
         _check_dispatch_tokens(w, case, g, dst, toks[c0:c0 + CHUNK_TOKENS], orc, check_row_w)
     if not check_empty:
-        return
+        return int(toks.size)
     # rows no entry maps to keep the sentinel (padding and empty slots)
     rows = ref["rows"]
     used = torch.zeros(max(rows, 1), dtype=torch.bool, device=g["out_rows"].device)
@@ -123,6 +124,7 @@ def check_dispatch(w, case, g, ref, sample_tokens=None, seed=0, orc=None, check_
             assert bool((buf.view(torch.int16) == SENTINEL_BF16).all())
         else:
             assert bool((buf == SENTINEL_U8).all())
+    return int(toks.size)
 
 
 def _check_dispatch_tokens(w, case, g, dst, toks, orc, check_row_w):

@@ -34,8 +34,8 @@ def test_workload_parity(name):
     g = gh.run_gpu(w, case)
     ref = gh.check_layout(w, case, g)
     assert ref["status"] == 0
-    gh.check_dispatch(w, case, g, ref)
-    frac = gh.check_combine(w, case, g, ref)
+    assert gh.check_dispatch(w, case, g, ref) == w.T  # every token's rows and scales
+    frac = gh.check_combine(w, case, g, ref)          # every token's output elements
     assert frac == 1.0, f"combine within 1 ulp but only {frac:.6f} bit-exact"
 
 
