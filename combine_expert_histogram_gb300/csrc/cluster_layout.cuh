@@ -140,7 +140,18 @@ __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_
         bad |= e0 < -1 || e0 >= E;
         const int e = (e0 >= 0 && e0 < E) ? e0 : E;  // E = no expert
         ev[r] = e;
-        const unsigned peers = __match_any_sync(kFullMask, e);
+        // lanes with the same expert: one ballot per bit of the id (E itself
+        // must fit); the ballots are independent, so their latencies overlap.
+        // In this latency-bound kernel (about one round per warp) they
+        // measured 0.2-0.35 us faster than one __match_any_sync, whose single
+        // result comes later; the tiled kernel's many rounds prefer the latter.
+        unsigned peers = kFullMask;
+        const int nbits = 32 - __clz(E);
+        for (int b = 0; b < nbits; ++b) {
+            const unsigned bit = (e >> b) & 1u;
+            const unsigned bal = __ballot_sync(kFullMask, bit);
+            peers &= bit ? bal : ~bal;
+        }
         const int before = e < E ? row[e] : 0;
         __syncwarp();
         if (e < E && lane == __ffs(peers) - 1) row[e] = before + __popc(peers);

@@ -8,10 +8,10 @@
 //
 // Design (deterministic, no global atomics on slot order; latency-bound, so
 // the goal is short dependency chains and many warps).  In both paths lanes
-// holding the same expert in a round of 32 entries find each other with one
-// __match_any_sync, and an entry's slot is the number of entries of its
-// expert before it: in lower CTAs or tiles, in lower warps, in earlier rounds
-// and in lower lanes -- exactly ascending (token, k) order.
+// holding the same expert in a round of 32 entries find each other (a peer
+// mask), and an entry's slot is the number of entries of its expert before
+// it: in lower CTAs or tiles, in lower warps, in earlier rounds and in lower
+// lanes -- exactly ascending (token, k) order.
 //
 //   * Up to 16384 entries (decode-sized batches): one kernel of one
 //     thread-block cluster (cluster_layout_kernel; its body is in
@@ -20,7 +20,8 @@
 //     after a cluster barrier reads its peers' histograms through distributed
 //     shared memory (four peers' loads in flight at once) for the expert
 //     totals and its slice's base.  No workspace, and no CTA reads more than
-//     its own slice of topk_idx; the CTAs share the row_src fill.
+//     its own slice of topk_idx; the CTAs share the row_src fill.  Peer masks
+//     from one ballot per bit of the id.
 //   * Beyond that: tile_hist_kernel counts each tile's experts (shared-memory
 //     atomics; counts need no order) into the workspace [tiles][E]; then
 //     assign_kernel, a programmatic dependent whose loads and match masks
@@ -29,9 +30,9 @@
 //     per-warp histograms into per-warp starting slots and writes the slots.
 //     Warp w of a tile's CTA owns a contiguous chunk of up to 256 entries,
 //     lane l holding entries chunk + 32r + l in registers (all loads issued
-//     up front).  One __match_any_sync per round replaced one __ballot_sync
-//     per bit of the id (601 k -> 384 k warp instructions, 14.0 -> 11.4 us
-//     for 65536 entries).  Extra CTAs of masked layouts with row_src only
+//     up front).  Peer masks from one __match_any_sync per round, which
+//     replaced one __ballot_sync per bit of the id here (601 k -> 384 k warp
+//     instructions, 14.0 -> 11.4 us for 65536 entries).  Extra CTAs of masked layouts with row_src only
 //     sum the expert totals and write -1 into row_src for empty slots.
 #include <stdlib.h>
 
