@@ -305,3 +305,19 @@ def test_combine_index_arrays_not_16_byte_aligned(shift):
     y_bits = gh.to_np_u16(y)
     expect = oracle.default().combine(y_bits, case["w"], dst, w.H)
     assert np.array_equal(gh.to_np_u16(out), expect)
+
+
+# row_src is optional: without it the cluster kernel runs one cluster with no
+# fill, and the tiled kernels no fill CTAs; every other array must be the same
+@pytest.mark.parametrize("name,T", [("qwen3_30b_a3b_decode", None), ("dsv3_decode", None),
+                                    ("skewed_zipf", 1500), ("dsv3_prefill", 3000)])
+def test_layout_without_row_src(name, T):
+    w = workloads.CONFIGS[name]
+    if T is not None:
+        w = w.with_(T=T, name=f"{name}_T{T}")
+    case = gh.make_case(w)
+    g = gh.run_gpu(w, case, with_row_src=False)
+    assert g["L"].row_src is None
+    ref = gh.check_layout(w, case, g)
+    gh.check_dispatch(w, case, g, ref)
+    assert gh.check_combine(w, case, g, ref) == 1.0
