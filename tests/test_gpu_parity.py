@@ -321,3 +321,25 @@ def test_layout_without_row_src(name, T):
     ref = gh.check_layout(w, case, g)
     gh.check_dispatch(w, case, g, ref)
     assert gh.check_combine(w, case, g, ref) == 1.0
+
+
+# rank_rows is optional as well (alone, and with row_src also absent)
+@pytest.mark.parametrize("T,layout,no_row_src", [(256, "masked", False), (256, "masked", True),
+                                                 (3000, "contig", False), (3000, "contig", True)])
+def test_layout_without_rank_rows(T, layout, no_row_src):
+    w = workloads.CONFIGS["skewed_zipf"].with_(T=T, H=128, layout=layout, cap=T,
+                                               name=f"no_rank_rows_{T}_{layout}")
+    case = gh.make_case(w)
+    L = ep.new_layout(w.T, w.K, w.E, w.layout, align=w.align, capacity=w.cap, num_ranks=w.R,
+                      with_row_src=not no_row_src)
+    L.rank_rows = None
+    L.status.fill_(7)
+    ep.ep_layout(case["idx_d"], w.E, out=L)
+    torch.cuda.synchronize()
+    ref = oracle.default().layout(case["idx"], w.E, w.layout, align=w.align, cap=w.cap, R=w.R)
+    assert int(L.status.item()) == ref["status"]
+    assert np.array_equal(L.expert_count.cpu().numpy(), ref["count"])
+    assert np.array_equal(L.expert_offset.cpu().numpy(), ref["offset"])
+    assert np.array_equal(L.dst_row.cpu().numpy().reshape(w.T, w.K), ref["dst_row"])
+    if L.row_src is not None:
+        assert np.array_equal(L.row_src.cpu().numpy()[:ref["rows"]], ref["row_src"])
