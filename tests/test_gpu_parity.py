@@ -325,7 +325,8 @@ def test_layout_without_row_src(name, T):
 
 # rank_rows is optional as well (alone, and with row_src also absent)
 @pytest.mark.parametrize("T,layout,no_row_src", [(256, "masked", False), (256, "masked", True),
-                                                 (3000, "contig", False), (3000, "contig", True)])
+                                                 (3000, "contig", False), (3000, "contig", True),
+                                                 (3000, "masked", False), (3000, "masked", True)])
 def test_layout_without_rank_rows(T, layout, no_row_src):
     w = workloads.CONFIGS["skewed_zipf"].with_(T=T, H=128, layout=layout, cap=T,
                                                name=f"no_rank_rows_{T}_{layout}")
