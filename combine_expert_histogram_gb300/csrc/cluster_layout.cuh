@@ -40,29 +40,23 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// The shared-memory word that `p` names, read from the CTAs of cluster ranks
-// c0 .. c0+3 (distributed shared memory), all four loads in flight at once.
-// Ranks at or past csize read rank 0 and give 0.
-__device__ __forceinline__ void ld_peers4(const int32_t *p, unsigned c0, unsigned csize,
-                                          int32_t v[4]) {
-    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
-    const unsigned r0 = c0 < csize ? c0 : 0, r1 = c0 + 1 < csize ? c0 + 1 : 0;
-    const unsigned r2 = c0 + 2 < csize ? c0 + 2 : 0, r3 = c0 + 3 < csize ? c0 + 3 : 0;
+// Shared-memory address `a` of this CTA, as the same address in the CTA of
+// cluster rank `rank` (distributed shared memory).
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, unsigned rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory at `src` to address `dst` of a peer CTA,
+// counted against the transaction bytes of the peer's barrier `bar` (both
+// already mapped to the peer).
+__device__ __forceinline__ void push_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                             uint32_t bar) {
     asm volatile(
-        "{\n\t.reg .b32 a0, a1, a2, a3;\n\t"
-        "mapa.shared::cluster.u32 a0, %4, %5;\n\t"
-        "mapa.shared::cluster.u32 a1, %4, %6;\n\t"
-        "mapa.shared::cluster.u32 a2, %4, %7;\n\t"
-        "mapa.shared::cluster.u32 a3, %4, %8;\n\t"
-        "ld.shared::cluster.s32 %0, [a0];\n\t"
-        "ld.shared::cluster.s32 %1, [a1];\n\t"
-        "ld.shared::cluster.s32 %2, [a2];\n\t"
-        "ld.shared::cluster.s32 %3, [a3];\n\t}"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
-        : "r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "r"(src), "r"(bytes), "r"(bar)
         : "memory");
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = c0 + j < csize ? v[j] : 0;
 }
 
 // v = -1 for rows [r0, r1) of row_src; 16-byte stores where the address allows.
@@ -96,27 +90,46 @@ __host__ __device__ inline int round_up_pow2(int v, int a) { return (v + a - 1) 
 // shared by the warps of all clusters (a second cluster spreads a large
 // masked fill over more SMs).
 //
+// The CTAs exchange their histograms by pushing: each CTA's one thread
+// bulk-copies its histogram block into a slot of every peer's shared memory,
+// and the copies complete on the peer's barrier, so every CTA waits for its
+// own incoming bytes only.  Measured against pulling the peers' words with
+// distributed-shared-memory loads after a cluster barrier (4-byte or 16-byte
+// loads, four peers at a time): 0.2 us faster at 8 CTAs and 2048 entries,
+// 0.45-0.9 us faster at 16 CTAs and 8192 entries.
+//
 // The body of a layout kernel of kClThreads threads per CTA: `csm` is
-// cluster_smem(E) bytes of the CTA's dynamic shared memory.  The caller has
-// waited for the previous kernel on the stream (griddepcontrol.wait) before
-// calling it; every thread of every CTA of the grid calls it.  Ends with a
-// cluster barrier.
+// cluster_smem(E) bytes of the CTA's dynamic shared memory (16-byte
+// aligned).  The caller has waited for the previous kernel on the stream
+// (griddepcontrol.wait) before calling it; every thread of every CTA of the
+// grid calls it.  Ends with a cluster barrier.
 template <int ROUNDS>
 __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_t *csm) {
     const int E = a.E;
-    int32_t *wh = csm;                  // [kClWarps][E] per-warp counts, then warp bases
-    int32_t *hist = wh + kClWarps * E;  // [E+1] this CTA's expert counts; [E] = bad-id flag
-    int32_t *tot = hist + E + 1;        // [E] expert totals
-    int32_t *base = tot + E;            // [E] entries of each expert in lower CTAs
-    int32_t *off = base + E;            // [E+1] first row of each expert
+    const int E4 = round_up_pow2(E, 4);  // whole 16-byte words of counts
+    const int HW = E4 + 4;               // words of a histogram block: counts, flag word, padding
+    int32_t *wh = csm;                   // [kClWarps][E] per-warp counts, then warp bases
+    int32_t *hist = wh + kClWarps * E;   // [HW] this CTA's block: counts (0 past E), [E4] bad-id flag
+    int32_t *tot = hist + HW;            // [E4] expert totals
+    int32_t *base = tot + E4;            // [E4] entries of each expert in lower CTAs
+    int32_t *off = base + E4;            // [E4 + 4] first row of each expert (E + 1 used)
+    int32_t *recv = off + E4 + 4;        // [kClMaxCtas][HW] the peers' blocks, by cluster rank
     __shared__ int32_t scan_tmp[kClWarps];
-    __shared__ int32_t s_flags;         // bit 0: a bad id; bit 1: a masked expert over capacity
+    __shared__ int32_t s_flags;  // bit 0: a bad id; 1: a masked expert over capacity; 2: timeout
+    __shared__ __align__(8) uint64_t s_bar;  // completes when every peer's block has arrived
 
     const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
     const bool writer = blockIdx.x < csize;  // cluster 0
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int w0 = ((int)crank * kClWarps + warp) * a.chunk;
     const int w1 = min(a.TK, w0 + a.chunk);
+    if (threadIdx.x == 0) {
+        mbar_init(&s_bar, 1);
+        mbar_init_fence();
+    }
+    // the barrier is initialised before any peer may push (the matching
+    // wait comes after the ranking, so this costs nothing)
+    cluster_arrive_relaxed();
 
     // 1. this warp's entries, all loads in flight at once; the warp zeroes
     //    its own count row meanwhile
@@ -160,49 +173,62 @@ __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_
     }
     bad = __syncthreads_or(bad);
 
-    // 3. warp counts -> warp bases within the CTA; the CTA's histogram
-    for (int e = threadIdx.x; e < E; e += kClThreads) {
+    // 3. warp counts -> warp bases within the CTA; the CTA's histogram block
+    for (int e = threadIdx.x; e < E4; e += kClThreads) {
         int run = 0;
+        if (e < E) {
 #pragma unroll
-        for (int w = 0; w < kClWarps; ++w) {
-            const int c = wh[w * E + e];
-            wh[w * E + e] = run;
-            run += c;
+            for (int w = 0; w < kClWarps; ++w) {
+                const int c = wh[w * E + e];
+                wh[w * E + e] = run;
+                run += c;
+            }
         }
         hist[e] = run;
     }
-    if (threadIdx.x == 0) hist[E] = bad;
+    if (threadIdx.x < 4) hist[E4 + threadIdx.x] = threadIdx.x == 0 ? bad : 0;
+    fence_proxy_async_smem();  // the block is read by the bulk copies below
+    __syncthreads();
 
-    // 4. every CTA's histogram is visible to the cluster; totals and this
-    //    CTA's base from all of them, plus the error flags
-    cluster_arrive();
-    cluster_wait();
+    // 4. push the block into slot crank of every peer; wait for the peers'
+    //    blocks; totals, this CTA's base and the error flags from them
+    cluster_wait();  // every peer's barrier is initialised
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)HW * sizeof(int32_t);
+        const uint32_t bar = smem_addr(&s_bar);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"(bytes * (csize - 1))
+                     : "memory");
+        const uint32_t src = smem_addr(hist), dst = smem_addr(recv + crank * HW);
+        for (unsigned p = 0; p < csize; ++p)
+            if (p != crank) push_to_peer(peer_addr(dst, p), src, bytes, peer_addr(bar, p));
+    }
+    int flags = mbar_wait(&s_bar, 0, nullptr) ? 0 : 4;
     const int cap = a.cap, masked = a.masked;
-    int flags = 0;
     for (int e = threadIdx.x; e < E; e += kClThreads) {
         int t = 0, b = 0;
-        for (unsigned c = 0; c < csize; c += 4) {
-            int v[4];
-            ld_peers4(hist + e, c, csize, v);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                t += v[j];
-                b += c + j < crank ? v[j] : 0;
-            }
+        for (unsigned c = 0; c < csize; ++c) {
+            const int v = c == crank ? hist[e] : recv[c * HW + e];
+            t += v;
+            b += c < crank ? v : 0;
         }
         tot[e] = t;
         base[e] = b;
         if (masked && t > cap) flags |= 2;
     }
-    if (threadIdx.x < csize) {
-        int v[4];
-        ld_peers4(hist + E, threadIdx.x, threadIdx.x + 1, v);  // peer threadIdx.x's flag
-        if (v[0]) flags |= 1;
-    }
-    // done reading the peers (nothing to publish: relaxed); they may exit
-    // once every thread of the cluster has arrived here
+    if (threadIdx.x < csize && (threadIdx.x == crank ? hist[E4] : recv[threadIdx.x * HW + E4]))
+        flags |= 1;
+    // every copy into this CTA has landed (nothing to publish: relaxed); the
+    // peers may exit once every thread of the cluster has arrived here, as
+    // then no copy still reads their shared memory
     cluster_arrive_relaxed();
     if (flags) atomicOr(&s_flags, flags);
+    // A timed-out wait (a bulk copy that never completed) reaches the status
+    // word from CTA 0 of cluster 0 through its flags, and from any other CTA
+    // as a raise: that comes a second after the exchange began, long after
+    // CTA 0 (which finished its own exchange, or it would report the
+    // timeout itself) wrote the word.
+    if (flags & 4) raise_status(a.status, EP_ERR_TIMEOUT);
 
     // 5. offsets: e*cap (masked) or the padded exclusive scan (contiguous)
     const int align = a.align;
@@ -239,7 +265,10 @@ __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_
         }
         if (crank == 0 && threadIdx.x == 0) {
             const int f = s_flags;
-            *a.status = (f & 1) ? EP_ERR_BAD_EXPERT_ID : (f & 2) ? EP_ERR_CAPACITY : EP_OK;
+            *a.status = (f & 4)   ? EP_ERR_TIMEOUT
+                        : (f & 1) ? EP_ERR_BAD_EXPERT_ID
+                        : (f & 2) ? EP_ERR_CAPACITY
+                                  : EP_OK;
         }
         if (crank == csize - 1) {
             if (threadIdx.x == 0) a.offset[E] = off[E];
@@ -266,14 +295,15 @@ __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_
             fill_minus_one(a.row_src, r0, r1, lane);
         }
     }
-    // no CTA leaves while a peer may still read its histogram
+    // no CTA leaves while a copy may still read its shared memory
     cluster_wait();
 }
 
 // Dynamic shared memory of the layout body: per-warp counts, the CTA's
-// histogram (+ bad-id flag), totals, bases and offsets.
+// histogram block, totals, bases, offsets and one block per possible peer.
 inline size_t cluster_smem(int E) {
-    return sizeof(int32_t) * ((size_t)kClWarps * E + 4 * (size_t)E + 2);
+    const size_t E4 = (size_t)round_up_pow2(E, 4), HW = E4 + 4;
+    return sizeof(int32_t) * ((size_t)kClWarps * E + HW + 2 * E4 + (E4 + 4) + kClMaxCtas * HW);
 }
 
 // CTAs of one cluster for TK entries with at most max_ctas per cluster, and
@@ -291,8 +321,9 @@ inline void cluster_shape(long long TK, int max_ctas, int *ctas, int *chunk) {
 }
 
 // Clusters needed for the row_src fill: one, or two to share a large masked
-// fill (the fill is bound by each SM's store rate, about 30 bytes per clock;
-// more than two clusters measured slower at the DeepSeek-V3 decode shape).
+// fill (the fill is bound by each SM's store rate, about 30 bytes per clock).
+// Measured at the DeepSeek-V3 decode shape: more than two clusters were not
+// faster, nor was filling by bulk copies from a block of -1 in shared memory.
 inline int fill_clusters(const ep_layout_t &L, int ctas) {
     if (L.kind != EP_LAYOUT_MASKED || L.row_src == nullptr) return 1;
     const long long rows = (long long)L.num_experts * L.capacity;

@@ -51,7 +51,6 @@ constexpr int kOutBufs = 4;               // FP8 output rows per CTA, at most
 constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory per CTA
 constexpr int kCopyMaxStages = 8;         // bf16 rows in flight per CTA, at most
 constexpr int kCopyBudget = 144 * 1024;   // bf16: shared memory per CTA aimed for
-constexpr long long kWaitLimit = 1LL << 31;  // SM clocks, about a second
 
 __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d) {
     // __nv_cvt_float2_to_fp8x2: round to nearest even, saturate to +-448;
@@ -59,10 +58,6 @@ __device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d) {
     const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
     const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
     return (lo & 0xffffu) | (hi << 16);
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
@@ -83,22 +78,8 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
-// Make this thread's generic-proxy shared-memory writes visible to the TMA (async proxy).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-                 : "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-// Make barrier initialisation visible to the other threads and to the TMA.
-__device__ __forceinline__ void mbar_init_fence() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    fence_proxy_async_smem();
 }
 // Start the row copy global -> shared: arrive on the barrier, announcing
 // `bytes` of transactions, and issue one bulk copy that completes them.
@@ -112,26 +93,6 @@ __device__ __forceinline__ void load_row(void *sdst, const void *gsrc, uint32_t 
             "r"(smem_addr(sdst)),
         "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
-}
-// Bounded wait for the phase of parity `parity` of a barrier (the phase
-// before the current one counts as complete): false once `limit` SM clocks
-// have passed, or as soon as *fail is set (when given).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *fail,
-                                          long long limit = kWaitLimit) {
-    const uint32_t a = smem_addr(bar);
-    const long long t0 = clock64();
-    for (;;) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((fail && *fail) || clock64() - t0 > limit) return false;
-    }
 }
 
 // Quantise one FP8 slot (16 consecutive elements a, b of group j/8, part

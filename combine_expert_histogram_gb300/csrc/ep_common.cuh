@@ -16,6 +16,48 @@ __device__ __forceinline__ void raise_status(int32_t *status, int code) {
     atomicMax(status, code);
 }
 
+// Every mbarrier wait in the library gives up after this many SM clocks
+// (about a second) and reports EP_ERR_TIMEOUT instead of hanging.
+constexpr long long kWaitLimit = 1LL << 31;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// Make this thread's generic-proxy shared-memory writes visible to the TMA (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+// Make barrier initialisation visible to the other threads (of the cluster)
+// and to the TMA.
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+}
+// Bounded wait for the phase of parity `parity` of a barrier (the phase
+// before the current one counts as complete): false once `limit` SM clocks
+// have passed, or as soon as *fail is set (when given).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *fail,
+                                          long long limit = kWaitLimit) {
+    const uint32_t a = smem_addr(bar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((fail && *fail) || clock64() - t0 > limit) return false;
+    }
+}
+
 __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));

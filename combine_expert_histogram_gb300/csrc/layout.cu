@@ -16,12 +16,12 @@
 //   * Up to 16384 entries (decode-sized batches): one kernel of one
 //     thread-block cluster (cluster_layout_kernel; its body is in
 //     cluster_layout.cuh).  Each CTA ranks its own slice of the entries with
-//     per-warp counts, publishes its expert histogram in shared memory, and
-//     after a cluster barrier reads its peers' histograms through distributed
-//     shared memory (four peers' loads in flight at once) for the expert
-//     totals and its slice's base.  No workspace, and no CTA reads more than
-//     its own slice of topk_idx; the CTAs share the row_src fill.  Peer masks
-//     from one ballot per bit of the id.
+//     per-warp counts and pushes its expert histogram into every peer's
+//     shared memory (one bulk copy per peer through distributed shared
+//     memory, completing on the peer's mbarrier); each CTA sums the blocks it
+//     received for the expert totals and its slice's base.  No workspace, and
+//     no CTA reads more than its own slice of topk_idx; the CTAs share the
+//     row_src fill.  Peer masks from one ballot per bit of the id.
 //   * Beyond that: tile_hist_kernel counts each tile's experts (shared-memory
 //     atomics; counts need no order) into the workspace [tiles][E]; then
 //     assign_kernel, a programmatic dependent whose loads and match masks
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kTileThreads) assign_kernel(AssignArgs a) {
 
 template <int ROUNDS>
 __global__ void __launch_bounds__(cl::kClThreads) cluster_layout_kernel(cl::ClusterArgs a) {
-    extern __shared__ int32_t csm[];
+    extern __shared__ __align__(16) int32_t csm[];
     // The layout's only kernel: wait for the previous kernel on the stream (it
     // may have produced topk_idx, and may still read these arrays) before
     // anything else; then the next kernel (dispatch) may start.

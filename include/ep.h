@@ -198,7 +198,10 @@ size_t ep_layout_workspace_bytes(const ep_layout_t *layout);
  * the layout and no workspace is needed; its cluster has 16 CTAs where the
  * device can co-schedule them, else 8.  The environment variable
  * EP_MAX_CLUSTER_CTAS=8 (read once per process) caps it at 8, for a device
- * partition that cannot place 16 co-scheduled CTAs.
+ * partition that cannot place 16 co-scheduled CTAs.  The cluster's CTAs
+ * exchange their histograms by bulk copies between their shared memories;
+ * should one never complete, the bounded wait raises EP_ERR_TIMEOUT and the
+ * layout's arrays are not valid.
  */
 ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *layout, void *workspace,
                       size_t workspace_bytes, ep_stream_t stream);
