@@ -1,5 +1,6 @@
 // The decode-sized layout (up to kClusterMaxEntries top-k entries) computed
-// by one thread-block cluster: the device body of the layout kernel in
+// by thread-block clusters in one kernel: one cluster ranks the entries, 1-3
+// more only count them.  The device body of the layout kernel in
 // csrc/layout.cu, and its host-side sizing and launch.
 //
 // The layout step that DeepEP V2's dispatch performs internally ("infers the
@@ -86,12 +87,11 @@ __host__ __device__ inline int round_up_pow2(int v, int a) { return (v + a - 1) 
 // entry order and the slot of an entry is
 //   (entries of its expert in lower CTAs) + (in lower warps of its CTA)
 //   + (in earlier rounds of its warp) + (in lower lanes of its round).
-// RANK clusters rank the entries and write dst_row and the valid row_src
-// rows; META clusters only count (shared-memory atomics) and write the
-// counts, offsets, status word and rank rows (the first META cluster) and
-// the -1 rows of row_src (all META clusters).  One cluster does both, or
-// cluster 0 ranks and 1-3 more do the rest: then the fill runs on more SMs
-// and in parallel with the slot writes (Qwen3-30B-A3B decode 3.02 -> 2.73 us,
+// Cluster 0 (RANK) ranks the entries and writes dst_row and the valid
+// row_src rows; the 1-3 clusters after it only count (shared-memory atomics)
+// and write the counts, offsets, status word and rank rows (cluster 1) and
+// the -1 rows of row_src (all of them).  So the fill runs on more SMs and in
+// parallel with the slot writes (Qwen3-30B-A3B decode 3.02 -> 2.73 us,
 // DeepSeek-V3 decode 4.23 -> 3.74 us against two clusters that both ranked
 // and shared the fill).
 //
@@ -109,7 +109,7 @@ __host__ __device__ inline int round_up_pow2(int v, int a) { return (v + a - 1) 
 // aligned).  The caller has waited for the previous kernel on the stream
 // (griddepcontrol.wait) before calling it; every thread of every CTA of the
 // grid calls it.  Ends with a cluster barrier.
-template <int ROUNDS, bool RANK, bool META>
+template <int ROUNDS, bool RANK>
 __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_t *csm) {
     const int E = a.E;
     const int E4 = round_up_pow2(E, 4);  // whole 16-byte words of counts
@@ -125,8 +125,8 @@ __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_
     __shared__ __align__(8) uint64_t s_bar;  // completes when every peer's block has arrived
 
     const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
-    constexpr bool writer = RANK, meta = META;
-    const bool meta_writer = META && (RANK || blockIdx.x / csize == 1);
+    constexpr bool writer = RANK, meta = !RANK;
+    const bool meta_writer = meta && blockIdx.x / csize == 1;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int w0 = ((int)crank * kClWarps + warp) * a.chunk;
     const int w1 = min(a.TK, w0 + a.chunk);
@@ -308,11 +308,10 @@ __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_
     }
 
     // 8. row_src = -1 on padding rows (contiguous) and empty slots (masked),
-    //    one warp per expert across the META clusters
+    //    one warp per expert across the counting clusters
     if (a.row_src && meta) {
-        const int first = RANK ? 0 : (int)csize;  // first filling CTA
-        const int gw = ((int)blockIdx.x - first) * kClWarps + warp;
-        const int nw = ((int)gridDim.x - first) * kClWarps;
+        const int gw = ((int)blockIdx.x - (int)csize) * kClWarps + warp;
+        const int nw = ((int)gridDim.x - (int)csize) * kClWarps;
         for (int e = gw; e < E; e += nw) {
             const int r0 = off[e] + (masked ? min(tot[e], cap) : tot[e]);
             const int r1 = masked ? off[e] + cap : off[e + 1];
@@ -347,14 +346,16 @@ inline void cluster_shape(long long TK, int max_ctas, int *ctas, int *chunk) {
 constexpr int kFillRowsPerCta = 2048;  // row_src rows a filling CTA is given, at most
 constexpr int kMaxMetaClusters = 3;
 
-// Clusters of the launch: one, or (with row_src) the ranking cluster plus
-// 1-3 clusters for the counts, offsets and the row_src fill, enough to give
-// each of their CTAs about kFillRowsPerCta rows of the largest possible fill
-// (E x capacity masked, E x (align - 1) padding rows contiguous).  The fill is
-// bound by each SM's store rate (about 30 bytes per clock), so it wants SMs;
-// off the ranking cluster it also no longer delays the slot writes' CTAs.
+// Clusters of the launch: the ranking cluster plus 1-3 counting clusters for
+// the counts, offsets, status and rank rows and the row_src fill, enough to
+// give each of their CTAs about kFillRowsPerCta rows of the largest possible
+// fill (E x capacity masked, E x (align - 1) padding rows contiguous; one
+// without row_src).  The fill is bound by each SM's store rate (about 30
+// bytes per clock), so it wants SMs; off the ranking cluster neither it nor
+// the metadata stores delay the slot writes (without row_src one counting
+// cluster measured 0.3 us faster than one cluster doing everything).
 inline int fill_clusters(const ep_layout_t &L, int ctas) {
-    if (L.row_src == nullptr) return 1;
+    if (L.row_src == nullptr) return 2;
     const long long rows = L.kind == EP_LAYOUT_MASKED
                                ? (long long)L.num_experts * L.capacity
                                : (long long)L.num_experts * (L.align - 1);

@@ -221,8 +221,8 @@ struct LayoutPlan {
     int grid;         // CTAs of the assign kernel (>= tiles; extra CTAs fill padding)
     size_t smem;      // dynamic shared memory of the assign kernel
     size_t ws_bytes;  // scratch: tiles x E int32 per-tile histograms (0 for the cluster kernel)
-    bool cluster;     // decode-sized: one kernel of one thread-block cluster (tiles = its CTAs,
-                      // for the largest cluster; the launch may use fewer, larger slices)
+    bool cluster;     // decode-sized: one kernel of thread-block clusters (tiles = the CTAs of
+                      // one, for the largest cluster; the launch may use fewer, larger slices)
 };
 LayoutPlan layout_plan(const ep_layout_t &L);
 // Every argument check of ep_layout except the workspace's, in its order.

@@ -13,16 +13,17 @@
 // it: in lower CTAs or tiles, in lower warps, in earlier rounds and in lower
 // lanes -- exactly ascending (token, k) order.
 //
-//   * Up to 16384 entries (decode-sized batches): one kernel of one
-//     thread-block cluster (cluster_layout_kernel; its body is in
-//     cluster_layout.cuh).  Each CTA ranks its own slice of the entries with
+//   * Up to 16384 entries (decode-sized batches): one kernel of 2-4
+//     thread-block clusters (cluster_layout_kernel; its body is in
+//     cluster_layout.cuh).  Each CTA of the first cluster ranks its own slice of the entries with
 //     per-warp counts and pushes its expert histogram into every peer's
 //     shared memory (one bulk copy per peer through distributed shared
 //     memory, completing on the peer's mbarrier); each CTA sums the blocks it
 //     received for the expert totals and its slice's base.  No workspace, and
-//     no CTA reads more than its own slice of topk_idx.  With row_src, 1-3
-//     more clusters that only count write the counts, offsets and status and
-//     share the row_src fill.  Peer masks from one ballot per bit of the id.
+//     no CTA reads more than its own slice of topk_idx.  This ranking
+//     cluster writes the slots; 1-3 more clusters that only count write the
+//     counts, offsets and status and share the row_src fill.  Peer masks from
+//     one ballot per bit of the id.
 //   * Beyond that: tile_hist_kernel counts each tile's experts (shared-memory
 //     atomics; counts need no order) into the workspace [tiles][E]; then
 //     assign_kernel, a programmatic dependent whose loads and match masks
@@ -295,12 +296,11 @@ __global__ void __launch_bounds__(kTileThreads) assign_kernel(AssignArgs a) {
     }
 }
 
-// ---- decode-sized batches: one thread-block cluster (cluster_layout.cuh) ----
+// ---- decode-sized batches: thread-block clusters (cluster_layout.cuh) ----
 
-// SPLIT: cluster 0 ranks and writes the slots, the other clusters write the
-// counts, offsets, status and rank rows and fill row_src; otherwise one
-// cluster does everything.
-template <int ROUNDS, bool SPLIT>
+// Cluster 0 ranks and writes the slots; the other clusters write the counts,
+// offsets, status and rank rows and fill row_src.
+template <int ROUNDS>
 __global__ void __launch_bounds__(cl::kClThreads) cluster_layout_kernel(cl::ClusterArgs a) {
     extern __shared__ __align__(16) int32_t csm[];
     // The layout's only kernel: wait for the previous kernel on the stream (it
@@ -308,27 +308,21 @@ __global__ void __launch_bounds__(cl::kClThreads) cluster_layout_kernel(cl::Clus
     // anything else; then the next kernel (dispatch) may start.
     pdl_wait();
     pdl_launch_dependents();
-    if constexpr (!SPLIT)
-        cl::cluster_layout_body<ROUNDS, true, true>(a, csm);
-    else if (blockIdx.x < cl::cluster_nctarank())
-        cl::cluster_layout_body<ROUNDS, true, false>(a, csm);
+    if (blockIdx.x < cl::cluster_nctarank())
+        cl::cluster_layout_body<ROUNDS, true>(a, csm);
     else
-        cl::cluster_layout_body<ROUNDS, false, true>(a, csm);
+        cl::cluster_layout_body<ROUNDS, false>(a, csm);
 }
 
 using ClusterKernel = void (*)(cl::ClusterArgs);
 
-template <bool SPLIT>
-ClusterKernel cluster_kernel_t(int rounds) {
+ClusterKernel cluster_kernel(int rounds) {
     switch (rounds) {
-        case 1: return cluster_layout_kernel<1, SPLIT>;
-        case 2: return cluster_layout_kernel<2, SPLIT>;
-        case 4: return cluster_layout_kernel<4, SPLIT>;
-        default: return cluster_layout_kernel<8, SPLIT>;
+        case 1: return cluster_layout_kernel<1>;
+        case 2: return cluster_layout_kernel<2>;
+        case 4: return cluster_layout_kernel<4>;
+        default: return cluster_layout_kernel<8>;
     }
-}
-ClusterKernel cluster_kernel(int rounds, bool split) {
-    return split ? cluster_kernel_t<true>(rounds) : cluster_kernel_t<false>(rounds);
 }
 
 }  // namespace
@@ -400,7 +394,7 @@ LayoutPlan layout_plan(const ep_layout_t &L) {
     const long long TK = (long long)L.num_tokens * L.num_topk;
     int warps;
     if (TK <= cl::kClusterMaxEntries) {
-        // one cluster (its CTA count is chosen at launch: 8 or 16 at most)
+        // clusters of up to 16 CTAs (the count is chosen at launch: 8 or 16 at most)
         int ctas, chunk;
         cl::cluster_shape(TK, cl::kClMaxCtas, &ctas, &chunk);
         p.cluster = true;
@@ -445,7 +439,7 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
     const int TK = L.num_tokens * L.num_topk;
     const int E = L.num_experts;
     if (p.cluster) {
-        const ClusterKernel probe = cluster_kernel(8, false);
+        const ClusterKernel probe = cluster_kernel(8);
         const int max_ctas =
             cl::max_cluster_ctas(reinterpret_cast<const void *>(probe), cl::cluster_smem(EP_MAX_EXPERTS));
         int ctas, chunk;
@@ -453,7 +447,7 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
         const cl::ClusterArgs c = cl::cluster_args(topk_idx, L, chunk);
         // the layout's only kernel: programmatic, waiting for the previous kernel first
         const int clusters = cl::fill_clusters(L, ctas);
-        return cl::launch_clusters(cluster_kernel(chunk / 32, clusters > 1), ctas, clusters,
+        return cl::launch_clusters(cluster_kernel(chunk / 32), ctas, clusters,
                                    cl::cluster_smem(E), stream, true, c);
     }
     AssignArgs a;
