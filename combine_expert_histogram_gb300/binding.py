@@ -55,7 +55,7 @@ _lib = None
 EXPORTS = ("ep_status_str", "ep_rows_capacity", "ep_scale_cols", "ep_scale_words",
            "ep_layout_workspace_bytes",
            "ep_layout", "ep_dispatch", "ep_layout_dispatch", "ep_combine", "ep_masked_repack",
-           "ep_layout_noalloc", "ep_selftest_bounded_wait",
+           "ep_layout_noalloc", "ep_selftest_bounded_wait", "ep_selftest_cluster_wait",
            "ep_rank_layout", "ep_rank_expand", "ep_route_topk")
 NOALLOC_SCRATCH_BYTES = 256 * 1024
 
@@ -99,6 +99,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ep_rank_expand.argtypes = [LP, LP, P, I32, ctypes.c_int, P, P, P, P, P]
     L.ep_selftest_bounded_wait.restype = ctypes.c_int
     L.ep_selftest_bounded_wait.argtypes = [P, I64, P]
+    L.ep_selftest_cluster_wait.restype = ctypes.c_int
+    L.ep_selftest_cluster_wait.argtypes = [P, I64, P]
     L.ep_layout_noalloc.restype = ctypes.c_int
     L.ep_layout_noalloc.argtypes = [P, LP, P]
     if path == LIB_PATH:
@@ -379,6 +381,15 @@ def ep_selftest_bounded_wait(status: torch.Tensor, limit_clocks: int, stream=Non
         raise ValueError("status must be a device int32 tensor")
     _check(load_library().ep_selftest_bounded_wait(_ptr(status), int(limit_clocks),
                                                     _stream(stream)), "ep_selftest_bounded_wait")
+
+
+def ep_selftest_cluster_wait(status: torch.Tensor, limit_clocks: int, stream=None) -> None:
+    """Make the cluster exchange's bounded wait run out in a 2-CTA cluster;
+    EP_ERR_TIMEOUT lands in ``status``."""
+    if status.dtype != torch.int32 or not status.is_cuda:
+        raise ValueError("status must be a device int32 tensor")
+    _check(load_library().ep_selftest_cluster_wait(_ptr(status), int(limit_clocks),
+                                                    _stream(stream)), "ep_selftest_cluster_wait")
 
 
 def ep_layout_noalloc(topk_idx: torch.Tensor, out: Layout, stream=None) -> Layout:

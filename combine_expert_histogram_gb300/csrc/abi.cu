@@ -191,6 +191,13 @@ ep_status_t ep_selftest_bounded_wait(int32_t *status, int64_t limit_clocks, ep_s
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_selftest_cluster_wait(int32_t *status, int64_t limit_clocks, ep_stream_t stream) {
+    if (!status || !aligned(status, 4) || limit_clocks < 1 || limit_clocks > (int64_t)1 << 31)
+        return EP_ERR_INVALID_ARG;
+    return from_cuda(launch_cluster_wait_selftest(status, (long long)limit_clocks,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 ep_status_t ep_combine(const ep_layout_t *L, const void *y, int32_t hidden, const float *topk_w,
                        void *out, ep_stream_t stream) {
     ep_status_t st = check_layout(L);

@@ -232,6 +232,8 @@ cudaError_t launch_layout(const int32_t *topk_idx, const ep_layout_t &L, int32_t
 
 // One CTA waiting on a barrier nothing completes, for at most limit_clocks.
 cudaError_t launch_wait_selftest(int32_t *status, long long limit_clocks, cudaStream_t stream);
+cudaError_t launch_cluster_wait_selftest(int32_t *status, long long limit_clocks,
+                                         cudaStream_t stream);
 // ep_layout followed by ep_dispatch, launched back to back.
 cudaError_t launch_layout_dispatch(const int32_t *topk_idx, const ep_layout_t &L,
                                    int32_t *workspace, const void *x, int H, ep_quant_t quant,

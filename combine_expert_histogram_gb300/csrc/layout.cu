@@ -389,6 +389,36 @@ int max_cluster_ctas(const void *func, size_t smem) {
 
 }  // namespace cl
 
+// Self-test of the cluster exchange's bounded wait: two CTAs of one cluster
+// initialise their barriers, meet at the cluster barrier and each wait for
+// 16 bytes that no peer sends (no copy is issued, so nothing can land after
+// the CTAs exit); each wait must give up after `limit` SM clocks, the CTAs
+// must still meet at the final cluster barrier, and the kernel must report
+// EP_ERR_TIMEOUT -- the same sequence as the layout's exchange.
+__global__ void __launch_bounds__(cl::kClThreads) cluster_wait_selftest_kernel(int32_t *status, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    cl::cluster_arrive_relaxed();
+    __syncthreads();
+    cl::cluster_wait();
+    if (threadIdx.x == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 16;" ::"r"(smem_addr(&bar))
+                     : "memory");
+    const bool ok = mbar_wait(&bar, 0, nullptr, limit);
+    cl::cluster_arrive_relaxed();
+    if (__syncthreads_or(!ok) && threadIdx.x == 0) raise_status(status, EP_ERR_TIMEOUT);
+    cl::cluster_wait();
+}
+
+cudaError_t launch_cluster_wait_selftest(int32_t *status, long long limit_clocks,
+                                         cudaStream_t stream) {
+    return cl::launch_clusters(cluster_wait_selftest_kernel, 2, 1, 0, stream, false, status,
+                               limit_clocks);
+}
+
 LayoutPlan layout_plan(const ep_layout_t &L) {
     LayoutPlan p{};
     const long long TK = (long long)L.num_tokens * L.num_topk;

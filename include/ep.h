@@ -274,6 +274,16 @@ ep_status_t ep_layout_dispatch(const int32_t *topk_idx, const ep_layout_t *layou
 ep_status_t ep_selftest_bounded_wait(int32_t *status, int64_t limit_clocks, ep_stream_t stream);
 
 /*
+ * ep_selftest_cluster_wait -- diagnostic with no counterpart in the pages:
+ * the same check for the bounded wait of the decode layout's histogram
+ * exchange.  Two CTAs of one thread-block cluster each wait for bytes no
+ * peer sends, for at most `limit_clocks` SM clocks (1 .. 2^31), still meet
+ * at the closing cluster barrier, and raise EP_ERR_TIMEOUT into *status
+ * (caller-owned, 4-byte aligned; its previous value is kept if larger).
+ */
+ep_status_t ep_selftest_cluster_wait(int32_t *status, int64_t limit_clocks, ep_stream_t stream);
+
+/*
  * ep_combine -- top-k weighted reduction back to token order ([VLLM-EP]
  * "weighted reduction in combine"; combine reuses the dispatch handle,
  * [PR-24443] "Motivation").  The reduction is applied exactly once.

@@ -155,3 +155,24 @@ def test_bounded_wait_gives_up_and_reports():
     assert L.dst_row.cpu().tolist() == ref["dst_row"].ravel().tolist()
     with pytest.raises(ep.EPError):
         ep.ep_selftest_bounded_wait(status, 0)  # limits outside 1 .. 2^31 are refused
+
+
+def test_cluster_bounded_wait_gives_up_and_reports():
+    """The decode layout's histogram exchange waits on a barrier for its
+    peers' bulk copies; that wait is bounded too: in a 2-CTA cluster whose
+    peers send nothing, both waits give up, the CTAs still meet at the
+    closing cluster barrier, EP_ERR_TIMEOUT lands in the status word, and the
+    context stays usable (a cluster layout runs and matches the oracle)."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_selftest_cluster_wait(status, 1 << 20)
+    torch.cuda.synchronize()
+    assert int(status.item()) == ep.EP_ERR_TIMEOUT
+    rng = np.random.default_rng(4)
+    idx = rng.integers(0, 64, size=(300, 8)).astype(np.int32)  # 2400 entries: cluster path
+    L = ep.ep_layout(torch.from_numpy(idx).cuda(), 64, kind="masked", capacity=300)
+    torch.cuda.synchronize()
+    ref = oracle.default().layout(idx, 64, "masked", cap=300)
+    assert int(L.status.item()) == ref["status"] == 0
+    assert np.array_equal(L.dst_row.cpu().numpy().reshape(idx.shape), ref["dst_row"])
+    with pytest.raises(ep.EPError):
+        ep.ep_selftest_cluster_wait(status, (1 << 31) + 1)
