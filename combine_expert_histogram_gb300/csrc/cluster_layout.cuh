@@ -271,7 +271,9 @@ __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_
                 int dst = -1;
                 if (e < E) {
                     const int slot = base[e] + row[e] + rank[r];
-                    if (!(masked && slot >= cap)) dst = off[e] + slot;
+                    // slot < tot[e] always holds unless the exchange timed out
+                    // (then the counts are garbage): no row outside the expert's
+                    if (slot < tot[e] && !(masked && slot >= cap)) dst = off[e] + slot;
                 }
                 a.dst_row[i] = dst;
                 if (dst >= 0 && a.row_src) a.row_src[dst] = i;

@@ -344,3 +344,18 @@ def test_layout_without_rank_rows(T, layout, no_row_src):
     assert np.array_equal(L.dst_row.cpu().numpy().reshape(w.T, w.K), ref["dst_row"])
     if L.row_src is not None:
         assert np.array_equal(L.row_src.cpu().numpy()[:ref["rows"]], ref["row_src"])
+
+
+# A large layout on the tiled path: 800000 entries at E = 1024, so 98 tiles
+# of four passes each (a histogram kernel and an assign kernel), contiguous
+# and masked (with row_src, so with fill CTAs)
+@pytest.mark.parametrize("layout", ["contig", "masked"])
+def test_tiled_layout_with_passes(layout):
+    w = workloads.Workload(f"tiled_{layout}", T=100000, H=128, E=1024, K=8, routing="softmax",
+                           layout=layout, quant="fp8_f32", align=128, cap=900, R=8, seed=31)
+    idx = np.random.default_rng(31).integers(-1, w.E, size=(w.T, w.K)).astype(np.int32)
+    case = _custom_case(w, idx)
+    g = gh.run_gpu(w, case)
+    ref = gh.check_layout(w, case, g)
+    gh.check_dispatch(w, case, g, ref, sample_tokens=2048)
+    assert gh.check_combine(w, case, g, ref, sample_tokens=2048) == 1.0

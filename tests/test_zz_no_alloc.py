@@ -94,7 +94,7 @@ def test_noalloc_masked_and_status_errors(cap, plant):
 def test_noalloc_argument_errors_match_ep_layout():
     """Bad arguments give ep_layout's code even when the shape is also too
     large for the fixed array: argument checks come first."""
-    T, K, E = 70000, 8, 1024
+    T, K, E = 100000, 8, 1024  # per-tile histograms: 98 tiles x 1024 experts x 4 B
     L = ep.new_layout(T, K, E, "contig", align=128)
     assert ep.ep_layout_workspace_bytes(L) > ep.NOALLOC_SCRATCH_BYTES
     lib = ep.load_library()
@@ -105,7 +105,7 @@ def test_noalloc_argument_errors_match_ep_layout():
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    T, K, E = 70000, 8, 1024  # 69 tiles x 1024 experts x 4 B > 256 KiB
+    T, K, E = 100000, 8, 1024  # 98 tiles x 1024 experts x 4 B > 256 KiB
     L = ep.new_layout(T, K, E, "contig", align=128)
     assert ep.ep_layout_workspace_bytes(L) > ep.NOALLOC_SCRATCH_BYTES
     idx = torch.zeros(T, K, dtype=torch.int32, device="cuda")
