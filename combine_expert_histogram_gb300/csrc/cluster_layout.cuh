@@ -32,9 +32,6 @@ __device__ __forceinline__ unsigned cluster_nctarank() {
     return r;
 }
 // All threads of every CTA of the cluster take part (uniform control flow).
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
@@ -244,9 +241,9 @@ __device__ __forceinline__ void cluster_layout_body(const ClusterArgs &a, int32_
     cluster_arrive_relaxed();
     if (flags) atomicOr(&s_flags, flags);
     // A timed-out wait (a bulk copy that never completed) reaches the status
-    // word from CTA 0 of cluster 0 through its flags, and from any other CTA
+    // word from CTA 0 of cluster 1 through its flags, and from any other CTA
     // as a raise: that comes a second after the exchange began, long after
-    // CTA 0 (which finished its own exchange, or it would report the
+    // that CTA (which finished its own exchange, or it would report the
     // timeout itself) wrote the word.
     if (flags & 4) raise_status(a.status, EP_ERR_TIMEOUT);
 
