@@ -617,6 +617,18 @@ def measure_decode(ep, dev, reps=50):
         torch.cuda.synchronize()
         step_us = graph_time_us([lay, dis, com], s, reps)
         one_call_us = graph_time_us([fus, com], s, reps)  # ep_layout_dispatch + ep_combine
+        # the same step with a layout that has no row_src (the masked decode
+        # path reads only dst_row and the counts)
+        Ln = ep.new_layout(w.T, w.K, w.E, "masked", capacity=w.cap, device=dev, with_row_src=False)
+        lay_n = lambda: ep.ep_layout(idx_d, w.E, out=Ln, stream=s)
+        dis_n = lambda: ep.ep_dispatch(Ln, x_d, w.quant, out_rows=out_rows, out_scales=sc, stream=s)
+        com_n = lambda: ep.ep_combine(Ln, y, w_d, out=out, stream=s)
+        with torch.cuda.stream(s):
+            lay_n(), dis_n(), com_n()
+        torch.cuda.synchronize()
+        step_n_us = graph_time_us([lay_n, dis_n, com_n], s, reps)
+        lay_n_warm = graph_time_us([lay_n], s, reps)
+        lay_n_cold = graph_time_us([lay_n], s, reps, flush=flush)
         cold = {k: graph_time_us([f], s, reps, flush=flush)
                 for k, f in (("layout", lay), ("dispatch", dis), ("combine", com))}
         warm = {k: graph_time_us([f], s, reps)
@@ -641,6 +653,9 @@ def measure_decode(ep, dev, reps=50):
             "step_us_graph": round(step_us, 2),
             "tokens_per_s": round(w.T / (step_us * 1e-6), 1),
             "step_us_graph_ep_layout_dispatch": round(one_call_us, 2),
+            "without_row_src": {"step_us_graph": round(step_n_us, 2),
+                                "layout_warm_us": round(lay_n_warm, 2),
+                                "layout_l2_flushed_us": round(lay_n_cold, 2)},
             "l2_flushed_us": {k: round(v, 2) for k, v in cold.items()},
             "warm_graph_us": {k: round(v, 2) for k, v in warm.items()},
             "dispatch_GBps_flushed": round(ab["dispatch"] / (cold["dispatch"] * 1e-6) / 1e9, 1),
