@@ -331,13 +331,14 @@ namespace cl {
 
 // EP_MAX_CLUSTER_CTAS=8 caps the cluster at the portable size (for a device
 // partition that cannot place 16 co-scheduled CTAs, or to check that
-// configuration); values below 8 count as 8, since the kernel's rounds per
-// warp allow at most 8 x 8 x 256 entries on 8 CTAs.
+// configuration).  The two sizes are the only ones used: any value below 16
+// counts as 8 (the kernel's rounds per warp allow at most 8 x 8 x 256
+// entries on 8 CTAs, so no fewer).
 int cluster_ctas_cap() {
     static const int cap = [] {
         const char *v = getenv("EP_MAX_CLUSTER_CTAS");
         const int n = v ? atoi(v) : kClMaxCtas;
-        return n < 8 ? 8 : n > kClMaxCtas ? kClMaxCtas : n;
+        return n < kClMaxCtas ? 8 : kClMaxCtas;
     }();
     return cap;
 }

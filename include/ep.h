@@ -197,8 +197,9 @@ size_t ep_layout_workspace_bytes(const ep_layout_t *layout);
  * Up to 16384 entries (T*K) one kernel of thread-block clusters computes
  * the layout and no workspace is needed; a cluster has 16 CTAs where the
  * device can co-schedule them, else 8.  The environment variable
- * EP_MAX_CLUSTER_CTAS=8 (read once per process) caps it at 8, for a device
- * partition that cannot place 16 co-scheduled CTAs.  A cluster's CTAs
+ * EP_MAX_CLUSTER_CTAS=8 (read once per process; any value below 16 counts
+ * as 8) caps it at 8, for a device partition that cannot place 16
+ * co-scheduled CTAs.  A cluster's CTAs
  * exchange their histograms by bulk copies between their shared memories;
  * should one never complete, the bounded wait raises EP_ERR_TIMEOUT and the
  * layout's arrays are not valid.

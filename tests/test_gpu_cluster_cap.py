@@ -1,7 +1,8 @@
-"""The cluster layout with its cluster capped at 8 CTAs (EP_MAX_CLUSTER_CTAS=8):
-up to 8 rounds of 32 entries per warp, the configuration of a device that
-cannot co-schedule 16 CTAs.  Run in a child process, since the cap is read
-once per process; the child compares every layout array with the oracle."""
+"""The cluster layout with its cluster capped at 8 CTAs (EP_MAX_CLUSTER_CTAS=8,
+and 12, which counts as 8): up to 8 rounds of 32 entries per warp, the
+configuration of a device that cannot co-schedule 16 CTAs.  Run in a child
+process, since the cap is read once per process; the child compares every
+layout array with the oracle."""
 import os
 import subprocess
 import sys
@@ -43,8 +44,9 @@ CHILD = textwrap.dedent("""
 """)
 
 
-def test_cluster_capped_at_8_ctas_matches_oracle():
-    env = dict(os.environ, EP_MAX_CLUSTER_CTAS="8")
+@pytest.mark.parametrize("cap", ["8", "12"])
+def test_cluster_capped_at_8_ctas_matches_oracle(cap):
+    env = dict(os.environ, EP_MAX_CLUSTER_CTAS=cap)
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], cwd=ROOT, env=env,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
