@@ -629,6 +629,28 @@ def measure_decode(ep, dev, reps=50):
         step_n_us = graph_time_us([lay_n, dis_n, com_n], s, reps)
         lay_n_warm = graph_time_us([lay_n], s, reps)
         lay_n_cold = graph_time_us([lay_n], s, reps, flush=flush)
+        # the step from router logits (fp32 [T, E], seeded N(0, 1), bias N(0, 0.1)):
+        # ep_route_topk, then the three calls on its topk_idx / topk_w
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(17)
+        lg = torch.randn((w.T, w.E), generator=gen, device=dev, dtype=torch.float32)
+        bias = 0.1 * torch.randn(w.E, generator=gen, device=dev, dtype=torch.float32)
+        idx_r = torch.empty((w.T, w.K), dtype=torch.int32, device=dev)
+        w_r = torch.empty((w.T, w.K), dtype=torch.float32, device=dev)
+        if w.routing == "softmax":
+            rte = lambda: ep.ep_route_topk(lg, w.K, "softmax", topk_idx=idx_r, topk_w=w_r,
+                                           stream=s)
+        else:
+            rte = lambda: ep.ep_route_topk(lg, w.K, "grouped_sigmoid", bias=bias,
+                                           n_group=w.n_group, topk_group=w.topk_group,
+                                           topk_idx=idx_r, topk_w=w_r, stream=s)
+        lay_r = lambda: ep.ep_layout(idx_r, w.E, out=L, stream=s)
+        com_r = lambda: ep.ep_combine(L, y, w_r, out=out, stream=s)
+        with torch.cuda.stream(s):
+            rte(), lay_r(), dis(), com_r()
+        torch.cuda.synchronize()
+        step_r_us = graph_time_us([rte, lay_r, dis, com_r], s, reps)
+        rte_us = graph_time_us([rte], s, reps)
         cold = {k: graph_time_us([f], s, reps, flush=flush)
                 for k, f in (("layout", lay), ("dispatch", dis), ("combine", com))}
         warm = {k: graph_time_us([f], s, reps)
@@ -653,6 +675,9 @@ def measure_decode(ep, dev, reps=50):
             "step_us_graph": round(step_us, 2),
             "tokens_per_s": round(w.T / (step_us * 1e-6), 1),
             "step_us_graph_ep_layout_dispatch": round(one_call_us, 2),
+            "from_logits": {"step_us_graph": round(step_r_us, 2),
+                            "router_us_graph": round(rte_us, 2),
+                            "what": "ep_route_topk + ep_layout + ep_dispatch + ep_combine"},
             "without_row_src": {"step_us_graph": round(step_n_us, 2),
                                 "layout_warm_us": round(lay_n_warm, 2),
                                 "layout_l2_flushed_us": round(lay_n_cold, 2)},

@@ -23,6 +23,21 @@ namespace {
 
 constexpr int kWarpsPerCta = 4;
 
+// Small router grids (at most one CTA per SM) are launched as programmatic
+// dependents and let the layout launch early; larger ones are launched
+// plainly and let it launch when they end.  Measured in CUDA-graph loops of
+// route + layout + dispatch + combine: 256 tokens (64 CTAs) 9.3 -> 8.7 us
+// with the early launches, while 1024 tokens (256 CTAs) went from 39.5 to
+// 40.7-42.7 us with either of them: a large grid resident early takes
+// registers that the still-running previous kernel's later waves need.
+// `early` is that choice; the wait comes first in both cases (without the
+// programmatic launch it returns at once): the previous kernel may have
+// produced the logits and may still read topk_idx / topk_w.
+__device__ __forceinline__ void route_pdl_prologue(bool early) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ bool ranks_before(float va, int a, float vb, int b) {
     return va > vb || (va == vb && a < b);
 }
@@ -54,8 +69,9 @@ template <int MODE>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     route_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T, int E,
                  int K, int n_group, int topk_group, int32_t *__restrict__ topk_idx,
-                 float *__restrict__ topk_w) {
+                 float *__restrict__ topk_w, bool early) {
     extern __shared__ float smem[];
+    route_pdl_prologue(early);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * kWarpsPerCta + warp;
     if (t >= T) return;  // whole warps
@@ -153,7 +169,8 @@ template <int VP, int MODE>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     route_reg_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int T,
                      int K, int n_group, int topk_group, int32_t *__restrict__ topk_idx,
-                     float *__restrict__ topk_w) {
+                     float *__restrict__ topk_w, bool early) {
+    route_pdl_prologue(early);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * kWarpsPerCta + warp;
     if (t >= T) return;  // whole warps
@@ -250,6 +267,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     }
 }
 
+// Programmatic launch and early trigger for grids of at most one CTA per SM.
+bool route_early(int grid) { return grid <= sm_count(); }
+
 template <int MODE>
 cudaError_t launch_reg(int VP, int grid, cudaStream_t stream, const float *logits,
                        const float *bias, int T, int K, int n_group, int topk_group,
@@ -257,9 +277,9 @@ cudaError_t launch_reg(int VP, int grid, cudaStream_t stream, const float *logit
     const int threads = kWarpsPerCta * 32;
 #define EP_ROUTE_CASE(V)                                                                      \
     case V:                                                                                   \
-        route_reg_kernel<V, MODE><<<grid, threads, 0, stream>>>(logits, bias, T, K, n_group, \
-                                                                topk_group, topk_idx, topk_w); \
-        break;
+        return launch_kernel(route_reg_kernel<V, MODE>, grid, threads, 0, stream,             \
+                             route_early(grid), logits, bias, T, K, n_group, topk_group,     \
+                             topk_idx, topk_w, route_early(grid));
     switch (VP) {
         EP_ROUTE_CASE(1)
         EP_ROUTE_CASE(2)
@@ -271,7 +291,6 @@ cudaError_t launch_reg(int VP, int grid, cudaStream_t stream, const float *logit
             return cudaErrorInvalidValue;
     }
 #undef EP_ROUTE_CASE
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -293,12 +312,12 @@ cudaError_t launch_route(const float *logits, const float *bias, int T, int E, i
     }
     const size_t smem = sizeof(float) * 2 * (size_t)E * kWarpsPerCta;
     if (mode == EP_ROUTE_SOFTMAX)
-        route_kernel<EP_ROUTE_SOFTMAX><<<grid, kWarpsPerCta * 32, smem, stream>>>(
-            logits, bias, T, E, K, n_group, topk_group, topk_idx, topk_w);
-    else
-        route_kernel<EP_ROUTE_GROUPED_SIGMOID><<<grid, kWarpsPerCta * 32, smem, stream>>>(
-            logits, bias, T, E, K, n_group, topk_group, topk_idx, topk_w);
-    return cudaGetLastError();
+        return launch_kernel(route_kernel<EP_ROUTE_SOFTMAX>, grid, kWarpsPerCta * 32, smem, stream,
+                             route_early(grid), logits, bias, T, E, K, n_group, topk_group, topk_idx,
+                             topk_w, route_early(grid));
+    return launch_kernel(route_kernel<EP_ROUTE_GROUPED_SIGMOID>, grid, kWarpsPerCta * 32, smem,
+                         stream, route_early(grid), logits, bias, T, E, K, n_group, topk_group,
+                         topk_idx, topk_w, route_early(grid));
 }
 
 }  // namespace ep
