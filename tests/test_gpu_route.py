@@ -104,22 +104,33 @@ def test_grouped_sigmoid_route(T, E, K, G, TG):
     assert in_kept[clear].all(), "a pick lies outside the kept groups"
 
 
-def test_route_then_layout_chain():
+# 2048 tokens: a router grid of 512 CTAs, launched plainly; 256 tokens: 64
+# CTAs, launched as a programmatic dependent that lets the layout launch
+# early (the layout reads topk_idx only after its own wait)
+@pytest.mark.parametrize("T,E,mode,layout", [(2048, 256, "grouped_sigmoid", "contig"),
+                                             (256, 128, "softmax", "masked")])
+def test_route_then_layout_chain(T, E, mode, layout):
     """Router output straight into layout, dispatch and combine (oracle on the same ids)."""
     from tests import gpu_harness as gh
     import workloads
-    T, E, K, H = 2048, 256, 8, 1024
+    K, H = 8, 1024
     rng = np.random.default_rng(3)
-    lg = rng.standard_normal((T, E)).astype(np.float32)
-    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
-    idx_d, w_d = ep.ep_route_topk(torch.from_numpy(lg).cuda(), K, "grouped_sigmoid",
-                                  bias=torch.from_numpy(bias).cuda(), n_group=8, topk_group=4)
-    w = workloads.Workload("chain", T=T, H=H, E=E, K=K, routing="grouped_sigmoid",
-                           layout="contig", quant="fp8_f32", align=128)
+    lg = torch.from_numpy(rng.standard_normal((T, E)).astype(np.float32)).cuda()
+    bias = torch.from_numpy((rng.standard_normal(E) * 0.1).astype(np.float32)).cuda()
+    w = workloads.Workload("chain", T=T, H=H, E=E, K=K, routing=mode, layout=layout,
+                           quant="fp8_f32", align=128, cap=T)
     x = workloads.make_x(w)
-    case = dict(idx=idx_d.cpu().numpy(), w=w_d.cpu().numpy(), x=x, idx_d=idx_d, w_d=w_d,
-                x_d=torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
+    x_d = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    # every input is on the device before the router runs, and nothing waits
+    # on the host between the router and the layout
+    if mode == "softmax":
+        idx_d, w_d = ep.ep_route_topk(lg, K, "softmax")
+    else:
+        idx_d, w_d = ep.ep_route_topk(lg, K, "grouped_sigmoid", bias=bias, n_group=8,
+                                      topk_group=4)
+    case = dict(x=x, idx_d=idx_d, w_d=w_d, x_d=x_d)
     g = gh.run_gpu(w, case)
+    case["idx"], case["w"] = idx_d.cpu().numpy(), w_d.cpu().numpy()
     ref = gh.check_layout(w, case, g)
     gh.check_dispatch(w, case, g, ref)
     assert gh.check_combine(w, case, g, ref) == 1.0
