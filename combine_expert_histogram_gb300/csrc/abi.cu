@@ -2,10 +2,27 @@
 // argument validation, sizing helpers and the launches.  Every host-detectable
 // error returns before anything is enqueued.
 #include <limits.h>
+#include <stdlib.h>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "ep_common.cuh"
 
 namespace ep {
+
+bool trace_enabled() {
+    static const bool on = [] {
+        const char *v = getenv("EP_NVTX");
+        return v != nullptr && atoi(v) != 0;
+    }();
+    return on;
+}
+TraceRange::TraceRange(const char *name) : on(trace_enabled()) {
+    if (on) nvtxRangePushA(name);
+}
+TraceRange::~TraceRange() {
+    if (on) nvtxRangePop();
+}
 
 int sm_count() {
     static int cached[64] = {0};
@@ -133,6 +150,7 @@ size_t ep_layout_workspace_bytes(const ep_layout_t *L) {
 
 ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *L, void *workspace,
                       size_t workspace_bytes, ep_stream_t stream) {
+    const TraceRange trace("ep_layout");
     const ep_status_t st = check_layout_call(topk_idx, L);
     if (st != EP_OK) return st;
     const LayoutPlan plan = layout_plan(*L);
@@ -146,6 +164,7 @@ ep_status_t ep_layout(const int32_t *topk_idx, const ep_layout_t *L, void *works
 ep_status_t ep_dispatch(const ep_layout_t *L, const void *x, int32_t hidden, ep_quant_t quant,
                         void *out_rows, void *out_scales, const float *topk_w, float *row_w,
                         ep_stream_t stream) {
+    const TraceRange trace("ep_dispatch");
     ep_status_t st = check_layout(L);
     if (st != EP_OK) return st;
     st = check_hidden(hidden, quant);
@@ -163,6 +182,7 @@ ep_status_t ep_layout_dispatch(const int32_t *topk_idx, const ep_layout_t *L, vo
                                size_t workspace_bytes, const void *x, int32_t hidden,
                                ep_quant_t quant, void *out_rows, void *out_scales,
                                const float *topk_w, float *row_w, ep_stream_t stream) {
+    const TraceRange trace("ep_layout_dispatch");
     // the argument rules of ep_layout and of ep_dispatch together
     ep_status_t st = check_layout(L);
     if (st != EP_OK) return st;
@@ -185,6 +205,7 @@ ep_status_t ep_layout_dispatch(const int32_t *topk_idx, const ep_layout_t *L, vo
 }
 
 ep_status_t ep_selftest_bounded_wait(int32_t *status, int64_t limit_clocks, ep_stream_t stream) {
+    const TraceRange trace("ep_selftest_bounded_wait");
     if (!status || !aligned(status, 4) || limit_clocks < 1 || limit_clocks > (int64_t)1 << 31)
         return EP_ERR_INVALID_ARG;
     return from_cuda(launch_wait_selftest(status, (long long)limit_clocks,
@@ -192,6 +213,7 @@ ep_status_t ep_selftest_bounded_wait(int32_t *status, int64_t limit_clocks, ep_s
 }
 
 ep_status_t ep_selftest_cluster_wait(int32_t *status, int64_t limit_clocks, ep_stream_t stream) {
+    const TraceRange trace("ep_selftest_cluster_wait");
     if (!status || !aligned(status, 4) || limit_clocks < 1 || limit_clocks > (int64_t)1 << 31)
         return EP_ERR_INVALID_ARG;
     return from_cuda(launch_cluster_wait_selftest(status, (long long)limit_clocks,
@@ -200,6 +222,7 @@ ep_status_t ep_selftest_cluster_wait(int32_t *status, int64_t limit_clocks, ep_s
 
 ep_status_t ep_combine(const ep_layout_t *L, const void *y, int32_t hidden, const float *topk_w,
                        void *out, ep_stream_t stream) {
+    const TraceRange trace("ep_combine");
     ep_status_t st = check_layout(L);
     if (st != EP_OK) return st;
     st = check_hidden(hidden, EP_QUANT_NONE);
@@ -214,6 +237,7 @@ ep_status_t ep_combine(const ep_layout_t *L, const void *y, int32_t hidden, cons
 ep_status_t ep_masked_repack(const ep_layout_t *L, const void *rows, const void *row_scales,
                              int32_t hidden, ep_quant_t quant, int32_t capacity, void *slab,
                              void *slab_scales, int32_t *masked_m, ep_stream_t stream) {
+    const TraceRange trace("ep_masked_repack");
     ep_status_t st = check_layout(L);
     if (st != EP_OK) return st;
     if (L->kind != EP_LAYOUT_CONTIG) return EP_ERR_INVALID_ARG;
@@ -233,6 +257,7 @@ ep_status_t ep_masked_repack(const ep_layout_t *L, const void *rows, const void 
 ep_status_t ep_route_topk(const float *logits, const float *bias, int32_t T, int32_t E,
                           int32_t K, ep_route_t mode, int32_t n_group, int32_t topk_group,
                           int32_t *topk_idx, float *topk_w, ep_stream_t stream) {
+    const TraceRange trace("ep_route_topk");
     if (T < 0 || E < 1 || E > EP_MAX_EXPERTS || K < 1 || K > EP_MAX_TOPK || K > E)
         return EP_ERR_INVALID_ARG;
     if (mode == EP_ROUTE_GROUPED_SIGMOID) {
@@ -255,6 +280,7 @@ ep_status_t ep_route_topk(const float *logits, const float *bias, int32_t T, int
 ep_status_t ep_rank_layout(const int32_t *topk_idx, int32_t num_experts, int32_t *rank_idx,
                            const ep_layout_t *RL, void *workspace, size_t workspace_bytes,
                            ep_stream_t stream) {
+    const TraceRange trace("ep_rank_layout");
     ep_status_t st = check_layout(RL);
     if (st != EP_OK) return st;
     if (RL->kind != EP_LAYOUT_CONTIG) return EP_ERR_INVALID_ARG;
@@ -275,6 +301,7 @@ ep_status_t ep_rank_expand(const ep_layout_t *RL, const ep_layout_t *L, const in
                            int32_t hidden, ep_quant_t quant, const void *send_rows,
                            const void *send_scales, void *out_rows, void *out_scales,
                            ep_stream_t stream) {
+    const TraceRange trace("ep_rank_expand");
     ep_status_t st = check_layout(RL);
     if (st != EP_OK) return st;
     st = check_layout(L);

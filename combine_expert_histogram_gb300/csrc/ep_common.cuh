@@ -178,6 +178,18 @@ __device__ __forceinline__ void block_exclusive_scan(int n, F value, int32_t *ou
 // Per-device properties, cached on first use (host side).
 int sm_count();
 
+// An NVTX range named after the entry point around every C-ABI call, when
+// the environment variable EP_NVTX=1 (read once per process); off by
+// default.  Without a tool attached (nsys, ncu) NVTX calls do nothing.
+bool trace_enabled();
+struct TraceRange {
+    explicit TraceRange(const char *name);
+    ~TraceRange();
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+    bool on;
+};
+
 // Let kernel `k` take `dynamic` bytes of dynamic shared memory.  Without an
 // explicit limit a CTA gets 48 KB of shared memory in all, the kernel's static
 // shared memory included, so the limit is raised whenever the two together

@@ -112,6 +112,7 @@ cudaError_t scratch_address(void **out) {
 
 extern "C" ep_status_t ep_layout_noalloc(const int32_t *topk_idx, const ep_layout_t *layout,
                                          ep_stream_t stream) {
+    const ep::TraceRange trace("ep_layout_noalloc");
     // ep_layout's own argument checks first, in its order, so that both calls
     // give the same code for the same bad arguments; the array's size next
     const ep_status_t st = ep::check_layout_call(topk_idx, layout);

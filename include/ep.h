@@ -41,6 +41,10 @@
  *     cudaDeviceGetAttribute) and, for ep_layout_noalloc alone, the fixed
  *     device array that call uses as scratch (with its looked-up address);
  *     every other entry point keeps nothing between calls.
+ *   - Tracing: with the environment variable EP_NVTX=1 (read once per
+ *     process) every entry point wraps its work in an NVTX range of its own
+ *     name, for nsys / ncu timelines; off by default, and the ranges do
+ *     nothing without a tool attached.
  *     Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and completes asynchronously.  Kernels are launched as
  *     programmatic dependents (programmatic dependent launch) and may start

@@ -139,3 +139,23 @@ def test_binding_refuses_cpu_tensors(lib):
     from combine_expert_histogram_gb300 import binding
     with pytest.raises(ValueError):
         binding._ptr(torch.zeros(4, dtype=torch.int32))
+
+
+def test_nvtx_ranges_around_a_call_that_returns_early(lib):
+    """EP_NVTX=1: the range around an entry point is pushed and popped also
+    when the call returns an argument error (no GPU needed)."""
+    import subprocess
+    import sys
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    child = ("import sys, ctypes; sys.path.insert(0, %r)\n"
+             "from combine_expert_histogram_gb300 import binding as b\n"
+             "lib = b.load_library()\n"
+             "L = b._Layout(); L.num_tokens = 4; L.num_topk = 2; L.num_experts = 8\n"
+             "L.num_ranks = 1; L.align = 1\n"
+             "assert lib.ep_layout(None, ctypes.byref(L), None, 0, None) == 1\n"
+             "assert lib.ep_combine(None, None, 128, None, None, None) == 1\n"
+             "print('ok')\n" % root)
+    r = subprocess.run([sys.executable, "-c", child], env=dict(os.environ, EP_NVTX="1"),
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
