@@ -538,9 +538,48 @@ def run_ours(args, w):
     if not args.skip_cpu and world == 1:  # the CPU baseline is an N=1 figure
         line["cpu_baseline"] = cpu_baseline(w, idx, wts, x)
         line["cpu_baseline_threads"] = cpu_baseline_threads(w, idx, wts, x)
+    if rank == 0:
+        print_table(line)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def print_table(line, out=None):
+    """A human-readable summary of the bench line on stderr (stdout keeps the
+    single JSON line): workload, per-kernel time, tokens/s, GB/s and fraction
+    of the HBM peak, the decode steps and the CPU oracle."""
+    out = out or sys.stderr
+    c = line.get("config", {})
+    rows = [("step (layout + dispatch + combine)", line.get("ms_per_step", 0) * 1e3,
+             line.get("value"), line.get("step_gbs"), None)]
+    T = c.get("T") or 0
+    for name, k in line.get("kernels", {}).items():
+        tps = k.get("tokens_per_s") or (T / (k["us"] * 1e-6) if k.get("us") else None)
+        rows.append((name, k.get("us"), tps, k.get("GB/s"), k.get("frac_of_peak")))
+
+    def fmt(v, f):
+        width = int("".join(ch for ch in f.split(".")[0] if ch.isdigit()) or 0)
+        return format("-", f">{width}") if v is None else format(v, f)
+    print(f"{c.get('workload', '?')}: T={c.get('T')} H={c.get('H')} E={c.get('E')} K={c.get('K')} "
+          f"quant={c.get('quant')}, peak {line.get('roofline', {}).get('peak')} GB/s "
+          f"({line.get('roofline', {}).get('peak_source')})", file=out)
+    print(f"  {'':36s} {'us':>9s} {'tokens/s':>12s} {'GB/s':>8s} {'of peak':>8s}", file=out)
+    for name, us, tps, gbs, frac in rows:
+        print(f"  {name:36s} {fmt(us, '9.2f')} {fmt(tps, '12.4g')} {fmt(gbs, '8.1f')} "
+              f"{fmt(frac, '8.3f')}", file=out)
+    for name, d in line.get("decode", {}).items():
+        print(f"  decode {name}: step {d['step_us_graph']} us from CUDA graphs "
+              f"(from logits {d.get('from_logits', {}).get('step_us_graph')} us); layout "
+              f"{d['warm_graph_us']['layout']} us warm", file=out)
+    for key in ("cpu_baseline", "cpu_baseline_threads"):
+        b = line.get(key)
+        if b:
+            print(f"  CPU oracle ({b['cores']} core{'s' if b['cores'] != 1 else ''}): "
+                  f"{b['value']:.4g} tokens/s", file=out)
+    e = line.get("e2e")
+    if e:
+        print(f"  end to end from pinned host memory: {e['value']:.4g} tokens/s", file=out)
 
 
 def graph_time_us(fns, stream, reps=50, flush=None, trials=5):

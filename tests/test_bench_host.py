@@ -43,3 +43,28 @@ def test_prefill_launch_bytes():
 def test_whole_job_tokens_per_s():
     # 4 replicas of 16384 tokens, 10 steps, slowest rank 5.0 ms in all
     assert bench.aggregate_tokens_per_s(16384, 10, 4, 5.0) == pytest.approx(16384 * 10 * 4 / 5e-3)
+
+
+def test_print_table_on_full_and_partial_lines():
+    """The stderr summary handles the fields a line may lack (no decode
+    section, no CPU baseline, kernels without a token rate)."""
+    import io
+    full = {"config": {"workload": "dsv3_prefill", "T": 16384, "H": 7168, "E": 256, "K": 8,
+                       "quant": "fp8_f32"},
+            "ms_per_step": 0.51, "value": 3.2e7, "step_gbs": 6500.0,
+            "roofline": {"peak": 6694.8, "peak_source": "measured"},
+            "kernels": {"layout": {"us": 14.2, "GB/s": 110.0, "frac_of_peak": 0.016},
+                        "combine": {"us": 309.0, "GB/s": 6840.0, "frac_of_peak": 1.02}},
+            "decode": {"qwen3_30b_a3b_decode": {"step_us_graph": 6.8,
+                                                "from_logits": {"step_us_graph": 8.7},
+                                                "warm_graph_us": {"layout": 2.7}}},
+            "cpu_baseline": {"value": 6000.0, "cores": 1},
+            "e2e": {"value": 1.3e6}}
+    buf = io.StringIO()
+    bench.print_table(full, out=buf)
+    text = buf.getvalue()
+    assert "dsv3_prefill" in text and "combine" in text and "from logits 8.7" in text
+    assert "CPU oracle (1 core)" in text and "end to end" in text
+    buf = io.StringIO()
+    bench.print_table({"config": {"workload": "tiny"}, "kernels": {"layout": {}}}, out=buf)
+    assert "tiny" in buf.getvalue()
