@@ -384,6 +384,14 @@ def pin_combine(orc, rng):
     none = (L["dst_row"] < 0).all(axis=1)
     if none.any():
         assert (out[none] == 0).all()
+    # (d) each product and each sum rounded to fp32 on its own (no fused
+    #     multiply-add): w = 1 + 2^-20 on +(1 + 2^-5) and -(1 + 2^-5) gives two
+    #     products whose fp32 rounding drops the same 2^-25, so they cancel to
+    #     exactly +0; a fused multiply-add would keep -2^-25 (a bf16 value)
+    y2 = torch_bf16_bits(np.array([[1 + 2.0 ** -5], [-(1 + 2.0 ** -5)]], dtype=np.float32))
+    w2 = np.full((1, 2), 1 + 2.0 ** -20, dtype=np.float32)
+    out2 = orc.combine(y2, w2, np.array([[0, 1]], dtype=np.int32), 1)
+    assert int(out2[0, 0]) == 0x0000
 
 
 def _within_bf16_ulp(out, exact, mag):

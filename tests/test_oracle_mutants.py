@@ -47,6 +47,8 @@ MUTANTS = {
     "ue8m0_pad_byte": ("eb[b] = 127;", "eb[b] = 0;"),
     "combine_dropped_term": ("acc = acc + p;", "acc = p;"),
     "combine_double_reduce": ("acc = acc + p;", "acc = acc + p + p;"),
+    "combine_fused_multiply_add": ("acc = acc + p;",
+                                   "acc = fmaf(topk_w[t * K + k], orc_bf16_to_float(y[(size_t)dst * H + h]), acc);"),
     "combine_transposed_w": ("float p = topk_w[t * K + k]", "float p = topk_w[k * T + t < T * K ? k * T + t : 0]"),
     "repack_masked_m_unclamped": ("masked_m[e] = n;", "masked_m[e] = count[e];"),
 }
