@@ -47,6 +47,11 @@ MUTANTS = {
     "ue8m0_pad_byte": ("eb[b] = 127;", "eb[b] = 0;"),
     "combine_dropped_term": ("acc = acc + p;", "acc = p;"),
     "combine_double_reduce": ("acc = acc + p;", "acc = acc + p + p;"),
+    "layout_bad_id_silent": ("if (status < ORC_BAD_EXPERT_ID) status = ORC_BAD_EXPERT_ID;", ";"),
+    "layout_rank_rows_shifted": ("for (int e = r * per; e < (r + 1) * per; ++e) s += count[e];",
+                                 "for (int e = r * per + 1; e <= (r + 1) * per && e < E; ++e) s += count[e];"),
+    "repack_slots_reversed": ("size_t src = (size_t)offset[e] + (size_t)s;",
+                              "size_t src = (size_t)offset[e] + (size_t)(n - 1 - s);"),
     "combine_fused_multiply_add": ("acc = acc + p;",
                                    "acc = fmaf(topk_w[t * K + k], orc_bf16_to_float(y[(size_t)dst * H + h]), acc);"),
     "combine_transposed_w": ("float p = topk_w[t * K + k]", "float p = topk_w[k * T + t < T * K ? k * T + t : 0]"),
