@@ -1033,6 +1033,24 @@ def measure_e2e(ep, w, L, idx, wts, x, y_dev, out_rows, out_scales, dev, stream,
     ms = t0.elapsed_time(t1) / n
     link = link_rates(h_x, bufs[0]["x"], up)
     link.update(numa_placement(h_x))
+    # one step's four uploads alone (no compute, no downloads), median of 5:
+    # the floor of the e2e step on this machine's host link
+    b = bufs[0]
+    t_up = []
+    for _ in range(5):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(up)
+        with torch.cuda.stream(up):
+            b["idx"].copy_(h_idx, non_blocking=True)
+            b["w"].copy_(h_w, non_blocking=True)
+            b["x"].copy_(h_x, non_blocking=True)
+            b["y"].copy_(h_y, non_blocking=True)
+        a1.record(up)
+        torch.cuda.synchronize()
+        t_up.append(a0.elapsed_time(a1))
+    up_ms = float(np.median(t_up))
+    link["step_uploads_ms"] = round(up_ms, 2)
+    link["step_uploads_GBps"] = round(h2d / (up_ms * 1e-3) / 1e9, 1)
     return {"value": w.T / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": n,
             "pipelined": "double-buffered inputs; copies up, compute, copies down overlap across steps",
