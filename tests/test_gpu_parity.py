@@ -359,3 +359,19 @@ def test_tiled_layout_with_passes(layout):
     ref = gh.check_layout(w, case, g)
     gh.check_dispatch(w, case, g, ref, sample_tokens=2048)
     assert gh.check_combine(w, case, g, ref, sample_tokens=2048) == 1.0
+
+
+# The two sides of the decode layout's limit: 16384 entries (the largest
+# cluster launch: 16 CTAs of 4 rounds per warp, with counting clusters) and
+# 16385 (the first tiled launch), masked with row_src and contiguous
+@pytest.mark.parametrize("T,K,layout", [(2048, 8, "masked"), (2048, 8, "contig"),
+                                        (3277, 5, "masked"), (3277, 5, "contig")])
+def test_layout_at_the_cluster_limit(T, K, layout):
+    w = workloads.Workload(f"limit_{T * K}_{layout}", T=T, H=256, E=96, K=K, routing="softmax",
+                           layout=layout, quant="fp8_ue8m0", align=64, cap=T, R=4, seed=51)
+    idx = np.random.default_rng(51 + T * K).integers(-1, w.E, size=(T, K)).astype(np.int32)
+    case = _custom_case(w, idx)
+    g = gh.run_gpu(w, case)
+    ref = gh.check_layout(w, case, g)
+    gh.check_dispatch(w, case, g, ref)
+    assert gh.check_combine(w, case, g, ref) == 1.0
